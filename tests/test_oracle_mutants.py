@@ -1,0 +1,85 @@
+"""Plant plausible mistakes in a private copy of the C oracle and check that the
+pins catch every one of them.
+
+Each mutant is the oracle source with one textual edit (a dropped term, a wrong
+index, a wrong reading of shard ownership), compiled to a temporary library on
+the CPU.  The pins of ``test_oracle_pins`` are run against it; at least one
+must fail.  The committed oracle is never modified.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+MUTANTS = {
+    "scale dropped": ("x[j] = scale * dot;", "x[j] = dot;"),
+    "no normalisation": ("orow[d] /= l;", "orow[d] /= 1.0;"),
+    "sum of weights wrong": ("l += x[j];", "l += x[j] * x[j];"),
+    "value row from the query index": ("const double* vj = vd + j * D;",
+                                       "const double* vj = vd + (j == 0 ? 0 : j - 1) * D;"),
+    "strided sequence ownership": ("idx4(b, p * Sl + s2, j, d, S, Hl, D)];\n    return 0;\n}\n\n/*\n * The inverse",
+                                   "idx4(b, s2 * P + p, j, d, S, Hl, D)];\n    return 0;\n}\n\n/*\n * The inverse"),
+    "local head index in the destination": (
+        "out[(size_t)(p * B * Sl * H * D) + idx4(b, s2, r * Hl + j, d, Sl, H, D)] =\n"
+        "                                L[",
+        "out[(size_t)(p * B * Sl * H * D) + idx4(b, s2, j * P + r, d, Sl, H, D)] =\n"
+        "                                L["),
+    "head shard takes the wrong head": ("o[idx4(b, s, r * Hl + j, d, S, H, D)];",
+                                        "o[idx4(b, s, j * P + r, d, S, H, D)];"),
+}
+
+PIN_CASES = [
+    (pins.test_worked_example_by_hand, ()),
+    (pins.test_reshard_index_table_by_hand, ()),
+    (pins.test_head_shards_hold_contiguous_head_ranges, ()),
+    (pins.test_brute_force_numpy, (8, 2)),
+    (pins.test_q_zero_gives_mean_of_v, (7,)),
+    (pins.test_weights_sum_to_one_and_match_output, ()),
+    (pins.test_key_permutation_invariance, ()),
+    (pins.test_reshard_of_one_hot_layout_inputs, ()),
+    (pins.test_torch_sdpa_fp64_crosscheck, ()),
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name!r} not unique"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", str(lib),
+                    str(path), "-lm"], check=True)
+    return str(lib)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path, monkeypatch):
+    lib_path = _build_mutant(tmp_path, name, *MUTANTS[name])
+    monkeypatch.setattr(oracle, "_LIB", lib_path)
+    monkeypatch.setattr(oracle, "_SRC", lib_path)  # keep build() from rebuilding
+    monkeypatch.setattr(oracle, "_lib", None)
+    failures = []
+    for fn, args in PIN_CASES:
+        try:
+            fn(*args)
+        except AssertionError:
+            failures.append(fn.__name__)
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert failures, f"no pin caught the mutant {name!r}"
+
+
+def test_unmutated_copy_passes_all_pins(tmp_path, monkeypatch):
+    src = open(oracle._SRC).read()
+    lib_path = _build_mutant(tmp_path, "identity", "double m = -INFINITY;", "double m = -INFINITY;")
+    monkeypatch.setattr(oracle, "_LIB", lib_path)
+    monkeypatch.setattr(oracle, "_SRC", lib_path)
+    monkeypatch.setattr(oracle, "_lib", None)
+    for fn, args in PIN_CASES:
+        fn(*args)
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert "double m = -INFINITY;" in src
+    assert isinstance(ctypes.CDLL(lib_path), ctypes.CDLL)
