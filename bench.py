@@ -1,0 +1,366 @@
+"""Benchmark: fused attention + Ulysses All-to-All layout on GB300.
+
+One step = one call of the fused path (attention over [B,S,H,D] with every
+output tile stored into its owner's sequence shard) on one batch of seeded
+synthetic bf16 input already resident in HBM.  Metric: TFLOP/s of the
+4*B*H*S^2*D tensor FLOPs, whole-job (summed over ranks).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload image]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+Prints ONE JSON line (rank 0).  Between timed steps the L2 cache is flushed by
+writing a 256 MiB buffer outside the timed events; each step is timed with CUDA
+events on the launching stream and the per-step times are summed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import dit_inputs as di  # noqa: E402
+
+DEFAULT_WORKLOAD = "image"
+METRIC = "fused attn+A2A-layout TFLOP/s and % of GB300 dense BF16 peak; fused-store overhead %"
+KERNEL_SOURCES = ["dit_attention_ulysses_gb300/csrc/attn_fwd.cu", "dit_attention_ulysses_gb300/csrc/ptx.cuh",
+                  "dit_attention_ulysses_gb300/csrc/kernels.h"]
+NCU_SUMMARY = os.path.join(ROOT, "profiles", "ncu_attn_a2a_kernel_image.txt")
+
+
+def env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    if it was taken on this workload and on the current kernel source."""
+    if not os.path.exists(NCU_SUMMARY):
+        return None
+    vals = {}
+    with open(NCU_SUMMARY) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash() or vals.get("workload") != workload:
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch_full_workload"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if t0 - 0.06 <= ts <= t1 + 0.06] or [r for _, r in rows[-3:]]
+        sm = [float(r[0]) for r in inside if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def to_device(bits, torch, dev):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def time_steps(torch, fn, steps, flush, stream):
+    """Run `steps` timed calls of fn with an L2 flush before each; returns per-step ms list."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.add_(1)
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def cpu_oracle_sample(w, seconds_target=12.0, max_rows=None):
+    """Time the fp64 oracle on a bounded sample of query rows (all heads) of workload w."""
+    import oracle
+    q, k, v = di.random_qkv(w)
+    threads = oracle.threads_used()
+    per_pair = 4.0 * w.S * w.D  # flops per (row, head)
+    # calibrate on a few rows, then size the sample for ~seconds_target
+    rb, rs = di.sample_rows(w, 8, seed=5)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, rb, rs)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    rate = len(rb) * w.H * per_pair / dt
+    n = int(seconds_target * rate / (w.H * per_pair))
+    n = max(8, min(n, w.B * w.S if max_rows is None else max_rows))
+    rb, rs = di.sample_rows(w, n, seed=6)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, rb, rs)
+    dt = time.perf_counter() - t0
+    flops = len(rb) * w.H * per_pair
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rb)} query rows x {w.H} heads of the {w.name} workload ({flops:.3e} FLOPs, "
+                      f"{dt:.1f} s, fp64 C/OpenMP)"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    w = di.WORKLOADS[args.workload]
+    q, k, v = di.random_qkv(w)
+    threads = oracle.threads_used()
+    rows_per_step = max(4, int(args.ref_rows))
+    per_pair = 4.0 * w.S * w.D
+    for i in range(args.warmup):
+        rb, rs = di.sample_rows(w, rows_per_step, seed=100 + i)
+        oracle.attention_rows(q, k, v, w.scale, rb, rs)
+    total_flops, total_t, n_rows = 0.0, 0.0, 0
+    for i in range(args.steps):
+        rb, rs = di.sample_rows(w, rows_per_step, seed=1000 + i)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.scale, rb, rs)
+        total_t += time.perf_counter() - t0
+        total_flops += len(rb) * w.H * per_pair
+        n_rows += len(rb)
+    value = total_flops / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "P": w.P,
+                   "sample": f"{rows_per_step} query rows x all heads per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_rows} query rows x {w.H} heads over {args.steps} steps"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import dit_attention_ulysses_gb300 as xs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = di.WORKLOADS[args.workload]
+    B, S, H, D, P = w.B, w.S, w.H, w.D, w.P
+    qb, kb, vb = di.random_qkv(w)
+    q, k, v = (to_device(x, torch, dev) for x in (qb, kb, vb))
+    shard_shape = (B, S // P, H, D)
+    outs = [torch.empty(shard_shape, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    contig = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+    heads = [torch.empty((B, S, H // P, D), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    serial = [torch.empty(shard_shape, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    fused = lambda: xs.xs_attn_a2a_fwd(q, k, v, outs, w.scale, stream)
+    alone = lambda: xs.xs_attn_fwd(q, k, v, contig, w.scale, stream)
+
+    def serial_path():
+        xs.xs_attn_heads_fwd(q, k, v, heads, w.scale, stream)
+        xs.xs_relayout_a2a(heads, serial, stream)
+
+    for _ in range(max(3, args.warmup)):
+        fused()
+    torch.cuda.synchronize()
+    if xs.xs_attn_get_device_error(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    per_step = time_steps(torch, fused, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+    status = xs.xs_attn_get_device_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device error status {status}")
+
+    total_ms = sum(per_step)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+
+    # ablation: attention alone (contiguous store) and attention + separate re-layout
+    n_abl = max(10, min(args.steps, 50))
+    for fn in (alone, serial_path):
+        for _ in range(3):
+            fn()
+    t_alone = statistics.median(time_steps(torch, alone, n_abl, flush, stream))
+    t_fused = statistics.median(time_steps(torch, fused, n_abl, flush, stream))
+    t_serial = statistics.median(time_steps(torch, serial_path, n_abl, flush, stream))
+
+    # end to end through the host-buffer entry point: H2D of q, k, v, kernel, D2H of the shards
+    pin = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).pin_memory()
+    qh, kh, vh = pin(qb), pin(kb), pin(vb)
+    out_h = [torch.empty(shard_shape, dtype=torch.bfloat16).pin_memory() for _ in range(P)]
+    e2e_fn = lambda: xs.xs_attn_a2a_fwd_staged(qh, kh, vh, out_h, q, k, v, outs, w.scale, stream)
+    for _ in range(2):
+        e2e_fn()
+    n_e2e = max(3, min(args.steps, 20))
+    e2e_ms = statistics.mean(time_steps(torch, e2e_fn, n_e2e, flush, stream))
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if xs.xs_attn_get_device_error(stream) != 0:
+        raise RuntimeError("device error after ablation / e2e runs")
+
+    if rank != 0:
+        return
+    peak_tflops, _, peak_kind = measured_peaks()
+    achieved = w.flops / (statistics.mean(per_step) * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "S": S, "H": H, "D": D, "P": P, "scale": w.scale,
+                   "inputs": "seeded bf16 N(0,1)" + (" with outlier channels" if w.outliers else ""),
+                   "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+                   "parallelism": f"{world} independent replica(s), one GPU each" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tflops if peak_tflops else None,
+                     "peak_kind": f"{peak_kind} bf16 burst",
+                     "traffic": ncu_traffic(w.name),
+                     "algorithmic_bytes": 4 * w.tensor_bytes},
+        "overhead_pct": 100.0 * (t_fused - t_alone) / t_alone,
+        "ablation": {"attention_alone_ms": t_alone, "fused_ms": t_fused, "attention_plus_relayout_ms": t_serial,
+                     "serial_over_fused": t_serial / t_fused, "runs": n_abl, "statistic": "median"},
+        "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 3 * w.tensor_bytes, "d2h_bytes_per_step": w.tensor_bytes,
+                "ms_per_step": e2e_ms, "api": "xs_attn_a2a_fwd_staged"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "kernel_source": kernel_source_hash(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_oracle_sample(w, seconds_target=args.cpu_seconds)
+    line["wall_s_timed_region"] = t_wall1 - t_wall0
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(di.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    args = ap.parse_args()
+    rank, world, local_rank = env_rank()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)   # rank 0 only; other ranks exit without work
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")   # barrier and max-over-ranks only; no data-path collective
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+"""Fused sequence-parallel attention + Ulysses All-to-All layout for GB300.
+
+Python binding of ``libxsattn.so`` (hand-written sm_103a CUDA kernels behind a
+C ABI, declared in ``include/xsattn.h``).  This module only marshals
+arguments: it turns torch tensors into pointers and sizes, picks the current
+CUDA stream, and raises :class:`XsError` on a non-zero return code.  Every
+step of the computation runs in the library's kernels; there is no fallback.
+PyTorch is used for device memory and streams only.
+
+Method: X-Stage (arXiv 2607.23264), abstract and the gist.science technical
+summary, "Key Contributions" item 3: the attention output-tile owner stores
+each finished tile straight into the post-attention Ulysses All-to-All layout
+(the sequence shard of the rank that owns the tile's rows) and resumes its next
+tile.  On one GPU the P ranks are P device buffers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "XsError",
+    "lib",
+    "xs_attn_a2a_fwd",
+    "xs_attn_fwd",
+    "xs_attn_heads_fwd",
+    "xs_relayout_a2a",
+    "xs_attn_a2a_fwd_staged",
+    "xs_attn_get_device_error",
+    "xs_attn_error_string",
+    "attn_a2a",
+    "LIB_PATH",
+    "EXPORTS",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libxsattn.so")
+
+# Error codes of include/xsattn.h
+XS_OK = 0
+XS_ERR_NULL = -1
+XS_ERR_SHAPE = -2
+XS_ERR_HEAD_DIM = -3
+XS_ERR_DIVISIBILITY = -4
+XS_ERR_TOO_MANY_RANKS = -5
+XS_ERR_ALIGNMENT = -6
+XS_ERR_OVERLAP = -7
+XS_ERR_SCALE = -8
+XS_ERR_CUDA = -9
+XS_ERR_DEVICE_TIMEOUT = -10
+XS_ERR_UNSUPPORTED_DEVICE = -11
+XS_MAX_P = 16
+
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+_f32 = ctypes.c_float
+
+# name -> (restype, argtypes); the full exported C ABI
+EXPORTS = {
+    "xs_attn_a2a_fwd": (_int, [_vp, _vp, _vp, ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32, _vp]),
+    "xs_attn_fwd": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _f32, _vp]),
+    "xs_attn_heads_fwd": (_int, [_vp, _vp, _vp, ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32, _vp]),
+    "xs_relayout_a2a": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _vp]),
+    "xs_attn_a2a_fwd_staged": (_int, [_vp, _vp, _vp, ctypes.POINTER(_vp), _vp, _vp, _vp, ctypes.POINTER(_vp),
+                                      _int, _int, _int, _int, _int, _f32, _vp]),
+    "xs_attn_get_device_error": (_int, [_vp]),
+    "xs_attn_error_string": (ctypes.c_char_p, [_int]),
+    "xs_attn_last_cuda_error": (_int, []),
+    "xs_attn_version": (_int, []),
+}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: the CUDA library has not been built "
+            "(run `python -c 'import __graft_entry__ as g; g.build()'`); there is no fallback")
+    handle = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in EXPORTS.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+lib = _load()
+
+
+class XsError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = lib.xs_attn_error_string(code).decode()
+        if code == XS_ERR_CUDA:
+            msg += f" (cudaError {lib.xs_attn_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{code}]")
+
+
+def _check(code: int, where: str) -> None:
+    if code != XS_OK:
+        raise XsError(code, where)
+
+
+def _ptr_array(ptrs):
+    arr = (_vp * max(1, len(ptrs)))()
+    for i, p in enumerate(ptrs):
+        arr[i] = p
+    return arr
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bshd(t, name):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+        raise TypeError(f"{name} must be a contiguous CUDA bfloat16 tensor [B,S,H,D]")
+    return t
+
+
+def xs_attn_a2a_fwd(q, k, v, out_ptrs, scale: float, stream=None) -> None:
+    """Fused attention; writes P sequence shards ``out_ptrs[p]`` of shape [B,S/P,H,D]."""
+    B, S, H, D = _bshd(q, "q").shape
+    _bshd(k, "k"), _bshd(v, "v")
+    outs = [_bshd(o, "out") for o in out_ptrs]
+    _check(lib.xs_attn_a2a_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr_array([o.data_ptr() for o in outs]),
+                               B, S, H, D, len(outs), scale, _stream_handle(stream)), "xs_attn_a2a_fwd")
+
+
+def xs_attn_fwd(q, k, v, out, scale: float, stream=None) -> None:
+    """Same attention kernel, one contiguous [B,S,H,D] output."""
+    B, S, H, D = _bshd(q, "q").shape
+    _bshd(k, "k"), _bshd(v, "v"), _bshd(out, "out")
+    _check(lib.xs_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, H, D, scale,
+                           _stream_handle(stream)), "xs_attn_fwd")
+
+
+def xs_attn_heads_fwd(q, k, v, heads, scale: float, stream=None) -> None:
+    """Same attention kernel, writing the P Ulysses head shards [B,S,H/P,D]."""
+    B, S, H, D = _bshd(q, "q").shape
+    _bshd(k, "k"), _bshd(v, "v")
+    hs = [_bshd(x, "heads") for x in heads]
+    _check(lib.xs_attn_heads_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr_array([x.data_ptr() for x in hs]),
+                                 B, S, H, D, len(hs), scale, _stream_handle(stream)), "xs_attn_heads_fwd")
+
+
+def xs_relayout_a2a(heads, out_ptrs, stream=None) -> None:
+    """Separate All-to-All re-layout: head shards [B,S,H/P,D] -> sequence shards [B,S/P,H,D]."""
+    hs = [_bshd(x, "heads") for x in heads]
+    outs = [_bshd(o, "out") for o in out_ptrs]
+    P = len(hs)
+    B, S, Hl, D = hs[0].shape
+    _check(lib.xs_relayout_a2a(_ptr_array([x.data_ptr() for x in hs]), _ptr_array([o.data_ptr() for o in outs]),
+                               B, S, Hl * P, D, P, _stream_handle(stream)), "xs_relayout_a2a")
+
+
+def xs_attn_a2a_fwd_staged(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, scale: float,
+                           stream=None) -> None:
+    """Host-resident variant: H2D copies, fused kernel and D2H copies of the shards, all on ``stream``."""
+    B, S, H, D = q_host.shape
+    P = len(out_dev)
+    _check(lib.xs_attn_a2a_fwd_staged(
+        q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), _ptr_array([o.data_ptr() for o in out_host]),
+        q_dev.data_ptr(), k_dev.data_ptr(), v_dev.data_ptr(), _ptr_array([o.data_ptr() for o in out_dev]),
+        B, S, H, D, P, scale, _stream_handle(stream)), "xs_attn_a2a_fwd_staged")
+
+
+def xs_attn_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status code."""
+    return lib.xs_attn_get_device_error(_stream_handle(stream))
+
+
+def xs_attn_error_string(code: int) -> str:
+    return lib.xs_attn_error_string(code).decode()
+
+
+def attn_a2a(q, k, v, P: int, scale: float | None = None, stream=None):
+    """Allocate the P output shards with torch and run the fused path; returns the list of shards."""
+    import torch
+    B, S, H, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    outs = [torch.empty((B, S // P, H, D), dtype=torch.bfloat16, device=q.device) for _ in range(P)]
+    xs_attn_a2a_fwd(q, k, v, outs, scale, stream)
+    return outs

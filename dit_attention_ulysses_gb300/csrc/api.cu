@@ -1,0 +1,324 @@
+// C ABI of the fused attention + Ulysses All-to-All layout library.
+//
+// Host-side argument validation (everything is checked before any CUDA call, so
+// an invalid call launches nothing), TMA tensor-map encoding, and launches.
+// The declarations and their contracts are in include/xsattn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/xsattn.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return XS_ERR_CUDA;
+}
+
+struct DeviceInfo {
+    bool known = false;
+    int sms = 0;
+    int major = 0;
+    int minor = 0;
+};
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[MAX_DEVICES];
+
+int device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= MAX_DEVICES) return XS_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.known) {
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        d.known = true;
+    }
+    *out = d;
+    if (d.major != 10 || d.minor != 3) return XS_ERR_UNSUPPORTED_DEVICE;
+    return XS_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::call_once(g_encode_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!g_encode) return cuda_fail(g_encode_err != cudaSuccess ? g_encode_err : cudaErrorSymbolNotFound);
+    *fn = g_encode;
+    return XS_OK;
+}
+
+// [B, S, H, D] bf16 as a 4-D tensor (D, H, S, B); box = 64 channels x 1 head x 128 rows.
+int encode_bshd(CUtensorMap* m, const void* base, int B, int S, int H, int D) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = get_encoder(&enc);
+    if (rc != XS_OK) return rc;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;
+    const cuuint64_t strides[3] = {row, row * H, row * H * S};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return XS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Shape checks shared by every attention entry point.
+int check_shape(int B, int S, int H, int D, int P, bool need_div) {
+    if (B < 1 || S < 1 || H < 1 || P < 1) return XS_ERR_SHAPE;
+    if (D != 64 && D != 128) return XS_ERR_HEAD_DIM;
+    if (P > XS_MAX_P) return XS_ERR_TOO_MANY_RANKS;
+    if (need_div && (S % P != 0 || H % P != 0)) return XS_ERR_DIVISIBILITY;
+    // sizes: elements per tensor and the work-unit count must fit the kernels' index types
+    const int64_t elems = static_cast<int64_t>(B) * S * H * D;
+    if (elems > (int64_t(1) << 40)) return XS_ERR_SHAPE;
+    const int64_t units = static_cast<int64_t>(B) * H * ((S + 255) / 256);
+    if (units > INT32_MAX) return XS_ERR_SHAPE;
+    return XS_OK;
+}
+
+int check_scale(float scale) {
+    if (!std::isfinite(scale) || scale < 0.0f) return XS_ERR_SCALE;
+    return XS_OK;
+}
+
+// Outputs must be pairwise disjoint and disjoint from every input.
+int check_disjoint(const Range* outs, int n_out, const Range* ins, int n_in) {
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlaps(outs[i], outs[j])) return XS_ERR_OVERLAP;
+        for (int j = 0; j < n_in; ++j)
+            if (overlaps(outs[i], ins[j])) return XS_ERR_OVERLAP;
+    }
+    return XS_OK;
+}
+
+Range range_of(const void* p, int64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+// Validation of (q, k, v, P output buffers of out_bytes each).
+int validate_attn(const void* q, const void* k, const void* v, void* const* outs, int n_out, int B, int S, int H,
+                  int D, int P, float scale, int64_t out_bytes, bool need_div) {
+    if (!q || !k || !v || !outs) return XS_ERR_NULL;
+    int rc = check_shape(B, S, H, D, P, need_div);
+    if (rc != XS_OK) return rc;
+    for (int i = 0; i < n_out; ++i)
+        if (!outs[i]) return XS_ERR_NULL;
+    if ((rc = check_scale(scale)) != XS_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return XS_ERR_ALIGNMENT;
+    for (int i = 0; i < n_out; ++i)
+        if (!aligned16(outs[i])) return XS_ERR_ALIGNMENT;
+    const int64_t in_bytes = static_cast<int64_t>(B) * S * H * D * 2;
+    Range ins[3] = {range_of(q, in_bytes), range_of(k, in_bytes), range_of(v, in_bytes)};
+    Range o[XS_MAX_P];
+    for (int i = 0; i < n_out; ++i) o[i] = range_of(outs[i], out_bytes);
+    return check_disjoint(o, n_out, ins, 3);
+}
+
+unsigned long long timeout_ns() {
+    return 1000000000ull;  // one second: no single wait in a healthy launch takes more than microseconds
+}
+
+int run_attention(const void* q, const void* k, const void* v, const xs::EpiParams& epi, int B, int S, int H, int D,
+                  float scale, cudaStream_t stream) {
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc != XS_OK) return rc;
+    CUtensorMap tq, tk, tv;
+    if ((rc = encode_bshd(&tq, q, B, S, H, D)) != XS_OK) return rc;
+    if ((rc = encode_bshd(&tk, k, B, S, H, D)) != XS_OK) return rc;
+    if ((rc = encode_bshd(&tv, v, B, S, H, D)) != XS_OK) return rc;
+    xs::AttnArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.n_kv = (S + 127) / 128;
+    a.n_qu = (S + 255) / 256;
+    a.units = B * H * a.n_qu;
+    a.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.epi = epi;
+    a.timeout_ns = timeout_ns();
+    const int grid = a.units < dev.sms ? a.units : dev.sms;
+    cudaError_t e = (D == 128) ? xs::launch_attn<128>(tq, tk, tv, a, grid, stream)
+                               : xs::launch_attn<64>(tq, tk, tv, a, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return XS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int xs_attn_a2a_fwd(const void* q, const void* k, const void* v, void* const* out_ptrs, int B, int S, int H, int D,
+                    int P, float scale, void* stream) {
+    if (!out_ptrs) return XS_ERR_NULL;
+    const int n_out = (P >= 1 && P <= XS_MAX_P) ? P : 0;
+    const int64_t shard_bytes = (P >= 1) ? static_cast<int64_t>(B) * (S / P) * H * D * 2 : 0;
+    int rc = validate_attn(q, k, v, out_ptrs, n_out, B, S, H, D, P, scale, shard_bytes, true);
+    if (rc != XS_OK) return rc;
+    xs::EpiParams epi;
+    std::memset(&epi, 0, sizeof epi);
+    for (int p = 0; p < P; ++p) epi.ptr[p] = out_ptrs[p];
+    epi.Sl = S / P;
+    epi.Hl = H;
+    return run_attention(q, k, v, epi, B, S, H, D, scale, static_cast<cudaStream_t>(stream));
+}
+
+int xs_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int S, int H, int D, float scale,
+                void* stream) {
+    void* outs[1] = {out};
+    const int64_t bytes = static_cast<int64_t>(B) * S * H * D * 2;
+    int rc = validate_attn(q, k, v, outs, 1, B, S, H, D, 1, scale, bytes, false);
+    if (rc != XS_OK) return rc;
+    xs::EpiParams epi;
+    std::memset(&epi, 0, sizeof epi);
+    epi.ptr[0] = out;
+    epi.Sl = S;
+    epi.Hl = H;
+    return run_attention(q, k, v, epi, B, S, H, D, scale, static_cast<cudaStream_t>(stream));
+}
+
+int xs_attn_heads_fwd(const void* q, const void* k, const void* v, void* const* heads, int B, int S, int H, int D,
+                      int P, float scale, void* stream) {
+    if (!heads) return XS_ERR_NULL;
+    const int n_out = (P >= 1 && P <= XS_MAX_P) ? P : 0;
+    const int64_t shard_bytes = (P >= 1) ? static_cast<int64_t>(B) * S * (H / P) * D * 2 : 0;
+    int rc = validate_attn(q, k, v, heads, n_out, B, S, H, D, P, scale, shard_bytes, true);
+    if (rc != XS_OK) return rc;
+    xs::EpiParams epi;
+    std::memset(&epi, 0, sizeof epi);
+    for (int p = 0; p < P; ++p) epi.ptr[p] = heads[p];
+    epi.Sl = S;
+    epi.Hl = H / P;
+    return run_attention(q, k, v, epi, B, S, H, D, scale, static_cast<cudaStream_t>(stream));
+}
+
+int xs_relayout_a2a(const void* const* heads, void* const* out_ptrs, int B, int S, int H, int D, int P,
+                    void* stream) {
+    if (!heads || !out_ptrs) return XS_ERR_NULL;
+    int rc = check_shape(B, S, H, D, P, true);
+    if (rc != XS_OK) return rc;
+    for (int p = 0; p < P; ++p)
+        if (!heads[p] || !out_ptrs[p]) return XS_ERR_NULL;
+    for (int p = 0; p < P; ++p)
+        if (!aligned16(heads[p]) || !aligned16(out_ptrs[p])) return XS_ERR_ALIGNMENT;
+    const int64_t head_bytes = static_cast<int64_t>(B) * S * (H / P) * D * 2;
+    const int64_t shard_bytes = static_cast<int64_t>(B) * (S / P) * H * D * 2;
+    Range ins[XS_MAX_P], outs[XS_MAX_P];
+    for (int p = 0; p < P; ++p) {
+        ins[p] = range_of(heads[p], head_bytes);
+        outs[p] = range_of(out_ptrs[p], shard_bytes);
+    }
+    if ((rc = check_disjoint(outs, P, ins, P)) != XS_OK) return rc;
+    DeviceInfo dev;
+    if ((rc = device_info(&dev)) != XS_OK) return rc;
+    xs::RelayoutArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int p = 0; p < P; ++p) {
+        a.heads[p] = heads[p];
+        a.out[p] = out_ptrs[p];
+    }
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.D = D;
+    a.P = P;
+    cudaError_t e = xs::launch_relayout(a, dev.sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return XS_OK;
+}
+
+int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v_host, void* const* out_host,
+                           void* q_dev, void* k_dev, void* v_dev, void* const* out_dev, int B, int S, int H, int D,
+                           int P, float scale, void* stream) {
+    if (!q_host || !k_host || !v_host || !out_host || !out_dev) return XS_ERR_NULL;
+    if (P >= 1 && P <= XS_MAX_P)
+        for (int p = 0; p < P; ++p)
+            if (!out_host[p]) return XS_ERR_NULL;
+    const int n_out = (P >= 1 && P <= XS_MAX_P) ? P : 0;
+    const int64_t shard_bytes = (P >= 1) ? static_cast<int64_t>(B) * (S / P) * H * D * 2 : 0;
+    int rc = validate_attn(q_dev, k_dev, v_dev, out_dev, n_out, B, S, H, D, P, scale, shard_bytes, true);
+    if (rc != XS_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t in_bytes = static_cast<size_t>(B) * S * H * D * 2;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(q_dev, q_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(k_dev, k_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(v_dev, v_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
+    if ((rc = xs_attn_a2a_fwd(q_dev, k_dev, v_dev, out_dev, B, S, H, D, P, scale, stream)) != XS_OK) return rc;
+    for (int p = 0; p < P; ++p)
+        if ((e = cudaMemcpyAsync(out_host[p], out_dev[p], static_cast<size_t>(shard_bytes), cudaMemcpyDeviceToHost,
+                                 st)) != cudaSuccess)
+            return cuda_fail(e);
+    return XS_OK;
+}
+
+int xs_attn_get_device_error(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    int v = 0;
+    if ((e = xs::read_and_clear_device_error(&v)) != cudaSuccess) return cuda_fail(e);
+    return v == 0 ? XS_OK : XS_ERR_DEVICE_TIMEOUT;
+}
+
+const char* xs_attn_error_string(int code) {
+    switch (code) {
+        case XS_OK: return "success";
+        case XS_ERR_NULL: return "a required pointer is NULL";
+        case XS_ERR_SHAPE: return "B, S, H and P must be >= 1 and the tensor sizes must fit the kernel's index types";
+        case XS_ERR_HEAD_DIM: return "head dimension D must be 64 or 128";
+        case XS_ERR_DIVISIBILITY: return "S and H must be divisible by the number of virtual ranks P";
+        case XS_ERR_TOO_MANY_RANKS: return "P exceeds XS_MAX_P (16)";
+        case XS_ERR_ALIGNMENT: return "device pointers must be 16-byte aligned";
+        case XS_ERR_OVERLAP: return "an output buffer overlaps another output or an input";
+        case XS_ERR_SCALE: return "scale must be finite and non-negative";
+        case XS_ERR_CUDA: return "a CUDA call or kernel launch failed (see xs_attn_last_cuda_error)";
+        case XS_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel expired; the launch was abandoned";
+        case XS_ERR_UNSUPPORTED_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
+        default: return "unknown xsattn error code";
+    }
+}
+
+int xs_attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int xs_attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -218,3 +218,38 @@ def sample_rows(w: Workload, n: int, seed: int = 1, S: int | None = None):
             picked.add(int(x))
     arr = np.array(sorted(picked), dtype=np.int64)
     return arr // S, arr % S
+
+
+def layout_code_inputs_torch(B: int, S: int, H: int, D: int, device="cuda"):
+    """The same index-coded (q, k, v, scale) as ``layout_code_inputs``, built
+    directly as bf16 torch tensors on ``device`` (for full-size cases, where the
+    NumPy construction would be slow).  Exact: every value is +-1 or an integer
+    below 256."""
+    import torch
+    nbits = _layout_nbits(S)
+    if nbits * LAYOUT_REP > D:
+        raise ValueError(f"S={S} needs {nbits * LAYOUT_REP} code channels > D={D}")
+    s = torch.arange(S, device=device, dtype=torch.int64)
+    code = torch.ones((S, D), device=device, dtype=torch.float32)
+    for i in range(nbits):
+        bit = ((s >> i) & 1).to(torch.float32) * 2.0 - 1.0
+        code[:, i * LAYOUT_REP:(i + 1) * LAYOUT_REP] = bit[:, None]
+    q = code.to(torch.bfloat16)[None, :, None, :].expand(B, S, H, D).contiguous()
+    k = q.clone()
+    v = layout_code_value_torch(B, S, H, D, device)
+    return q, k, v, 16.0
+
+
+def layout_code_value_torch(B: int, S: int, H: int, D: int, device="cuda", s_offset: int = 0, S_rows=None):
+    """bf16 tensor [B, S_rows, H, D] holding the index code of rows
+    s_offset .. s_offset + S_rows - 1 (see ``layout_code_value``)."""
+    import torch
+    n = S if S_rows is None else S_rows
+    s = torch.arange(s_offset, s_offset + n, device=device, dtype=torch.int64)
+    v = (torch.arange(D, device=device, dtype=torch.int64) % 256).to(torch.float32)
+    v = v.expand(B, n, H, D).clone()
+    v[..., 0] = (s % 256).to(torch.float32)[None, :, None]
+    v[..., 1] = ((s // 256) % 256).to(torch.float32)[None, :, None]
+    v[..., 2] = (torch.arange(H, device=device) % 256).to(torch.float32)[None, None, :]
+    v[..., 3] = (torch.arange(B, device=device) % 256).to(torch.float32)[:, None, None]
+    return v.to(torch.bfloat16)

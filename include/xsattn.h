@@ -1,0 +1,157 @@
+/*
+ * xsattn: fused sequence-parallel attention + post-attention Ulysses All-to-All
+ * layout for one GB300 (sm_103a).
+ *
+ * The method (X-Stage, arXiv 2607.23264, abstract; gist.science technical
+ * summary, "Key Contributions" item 3, "FlashAttention-A2A (Piggybacking)"):
+ * in Ulysses sequence-parallel DiT attention, the output-tile owner of the
+ * attention kernel writes every finished output tile straight to the rank that
+ * owns the tile's sequence block, then goes on to the next tile's Q-loop, so no
+ * separate All-to-All (transpose / copy) step runs after attention.
+ *
+ * On one GPU the P ranks are "virtual": P plain device buffers.  Shard p owns the
+ * contiguous sequence block [p*S/P, (p+1)*S/P) and holds all H heads at their
+ * global head index.
+ *
+ * Layout conventions (all entry points):
+ *   - bf16 tensors, row-major [B, S, H, D] with D fastest ("BSHD"), contiguous.
+ *   - Attention is bidirectional (non-causal): O = softmax(Q K^T * scale) V per
+ *     (b, h), no mask, no bias, no dropout.  Accumulation is fp32, the
+ *     probabilities are rounded to bf16 before the PV product, the output is
+ *     rounded to bf16 (round to nearest even).
+ *   - D must be 64 or 128.  S, B, H >= 1; S need not be a multiple of the tile.
+ *   - All device pointers must be 16-byte aligned.
+ *
+ * Ownership and synchronisation:
+ *   - The caller owns every buffer and the stream.  The library allocates no
+ *     device memory per call; it keeps one device error word per process.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Outputs are valid once the stream reaches the end of
+ *     the call.  Inputs are never modified.
+ *   - Host pointer arrays (out_ptrs, heads) are read before the call returns;
+ *     the library keeps no reference to them.
+ *
+ * Errors: every entry point returns XS_OK (0) or a negative XS_ERR_* code.
+ * Argument checks run on the host before anything is launched; a failed check
+ * launches nothing.  NaN/Inf in the inputs give undefined (but memory-safe)
+ * results.
+ */
+#ifndef XSATTN_H
+#define XSATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Maximum number of virtual ranks (output shards). */
+#define XS_MAX_P 16
+
+enum {
+    XS_OK = 0,
+    XS_ERR_NULL = -1,            /* a required pointer is NULL                         */
+    XS_ERR_SHAPE = -2,           /* B, S, H or P < 1, or a size overflows               */
+    XS_ERR_HEAD_DIM = -3,        /* D is not 64 or 128                                  */
+    XS_ERR_DIVISIBILITY = -4,    /* S % P != 0 or H % P != 0                            */
+    XS_ERR_TOO_MANY_RANKS = -5,  /* P > XS_MAX_P                                        */
+    XS_ERR_ALIGNMENT = -6,       /* a device pointer is not 16-byte aligned             */
+    XS_ERR_OVERLAP = -7,         /* an output buffer overlaps another output or input   */
+    XS_ERR_SCALE = -8,           /* scale is NaN or infinite                            */
+    XS_ERR_CUDA = -9,            /* a CUDA runtime/driver call or launch failed         */
+    XS_ERR_DEVICE_TIMEOUT = -10, /* a bounded wait inside a kernel ran out; see below   */
+    XS_ERR_UNSUPPORTED_DEVICE = -11 /* the current device is not sm_103 (GB300)        */
+};
+
+/*
+ * xs_attn_a2a_fwd -- the fused path.
+ *
+ * Computes O = softmax(Q K^T * scale) V for q, k, v of shape [B,S,H,D] and stores
+ * every output row (b, s, h) directly into the sequence shard of its owner:
+ *     p  = s / (S/P),   s' = s - p*(S/P)
+ *     out_ptrs[p][b, s', h, :]   (each out_ptrs[p] is a [B, S/P, H, D] bf16 buffer)
+ * This is the layout the post-attention Ulysses All-to-All produces (X-Stage,
+ * abstract: tile-granular fusion of the post-attention All-to-All with
+ * FlashAttention; the output-tile owner issues the stores and resumes the next
+ * tile).  Every element of every shard is written exactly once.
+ *
+ *   q, k, v   device, bf16 [B,S,H,D], read only.
+ *   out_ptrs  host array of P device pointers, each a distinct [B,S/P,H,D] bf16
+ *             buffer that must not overlap q, k, v or another shard.
+ *   P         1 <= P <= XS_MAX_P, S % P == 0, H % P == 0.
+ *   scale     finite softmax scale (1/sqrt(D) for standard attention).
+ *   stream    cudaStream_t to launch on.
+ */
+int xs_attn_a2a_fwd(const void* q, const void* k, const void* v, void* const* out_ptrs,
+                    int B, int S, int H, int D, int P, float scale, void* stream);
+
+/*
+ * xs_attn_fwd -- the same attention kernel storing one contiguous [B,S,H,D]
+ * output ("attention alone").  The arithmetic is identical to xs_attn_a2a_fwd;
+ * only the destination address of each output row differs, so
+ * out[b, p*S/P + s', h] == out_ptrs[p][b, s', h] bit for bit.
+ */
+int xs_attn_fwd(const void* q, const void* k, const void* v, void* out,
+                int B, int S, int H, int D, float scale, void* stream);
+
+/*
+ * xs_attn_heads_fwd -- the same attention kernel storing the head shards a
+ * Ulysses rank holds before the post-attention All-to-All:
+ *     r = h / (H/P), j = h % (H/P),   heads[r][b, s, j, :]
+ * each heads[r] a [B, S, H/P, D] bf16 buffer.  Together with xs_relayout_a2a
+ * this is the unfused "serial" path: attention, then a separate exchange.
+ */
+int xs_attn_heads_fwd(const void* q, const void* k, const void* v, void* const* heads,
+                      int B, int S, int H, int D, int P, float scale, void* stream);
+
+/*
+ * xs_relayout_a2a -- the separate All-to-All re-layout kernel (single GPU):
+ *     out_ptrs[p][b, s', r*(H/P) + j, :] = heads[r][b, p*(S/P) + s', j, :]
+ * heads: host array of P device pointers to [B,S,H/P,D] bf16 buffers;
+ * out_ptrs: host array of P device pointers to [B,S/P,H,D] bf16 buffers.
+ * Outputs must not overlap the inputs or each other.  Pure data movement,
+ * 16-byte vector copies; bit-exact.
+ */
+int xs_relayout_a2a(const void* const* heads, void* const* out_ptrs,
+                    int B, int S, int H, int D, int P, void* stream);
+
+/*
+ * xs_attn_a2a_fwd_staged -- xs_attn_a2a_fwd for host-resident data.
+ * Copies q, k, v from host memory (pinned for asynchronous copies) into the
+ * caller's device buffers q_dev, k_dev, v_dev, runs the fused kernel into the
+ * caller's device shards out_dev[p], and copies every shard back into the host
+ * buffers out_host[p]; all on `stream`, in that order.  The host buffers must
+ * stay alive and untouched until the stream has finished.  Device-side rules
+ * are those of xs_attn_a2a_fwd.
+ */
+int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v_host,
+                           void* const* out_host,
+                           void* q_dev, void* k_dev, void* v_dev, void* const* out_dev,
+                           int B, int S, int H, int D, int P, float scale, void* stream);
+
+/*
+ * xs_attn_get_device_error -- synchronises `stream`, then reads and clears the
+ * library's device error word on the current device.  Returns XS_OK, or
+ * XS_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel expired (the kernel
+ * then abandoned its work and returned; its outputs are unspecified), or
+ * XS_ERR_CUDA if synchronisation itself failed.
+ */
+int xs_attn_get_device_error(void* stream);
+
+/* Human-readable text for an XS_* code (static storage; never NULL). */
+const char* xs_attn_error_string(int code);
+
+/*
+ * The most recent CUDA error seen by the library on this thread (a
+ * cudaError_t value; 0 if none), for reports after XS_ERR_CUDA.
+ */
+int xs_attn_last_cuda_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int xs_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XSATTN_H */

@@ -1,0 +1,63 @@
+"""Full-size workloads, in the launch configuration the benchmark times.
+
+For every workload: the index-coded layout test bit for bit over every element
+of every shard, and random data against the fp64 oracle on a seeded sample of
+query rows (all heads, every shard's first and last row included).
+"""
+import numpy as np
+import pytest
+
+import dit_inputs as di
+from _parity import abs_bits, assert_close, bits_to_torch, torch_to_f64
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+FULL = ["tiny", "image", "video_small", "video_large", "sweep_S1024", "sweep_S8192", "sweep_S131072"]
+ROWS = {"tiny": 256, "image": 192, "video_small": 96, "video_large": 48,
+        "sweep_S1024": 128, "sweep_S8192": 96, "sweep_S131072": 24}
+
+
+@pytest.fixture(scope="module")
+def xs():
+    from conftest import build_library
+    build_library()
+    import dit_attention_ulysses_gb300 as xs
+    return xs
+
+
+def _shards(w):
+    return [torch.empty((w.B, w.S // w.P, w.H, w.D), dtype=torch.bfloat16, device="cuda") for _ in range(w.P)]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_layout_bit_exact_full(xs, name):
+    w = di.WORKLOADS[name]
+    q, k, v, scale = di.layout_code_inputs_torch(w.B, w.S, w.H, w.D)
+    outs = _shards(w)
+    xs.xs_attn_a2a_fwd(q, k, v, outs, scale)
+    torch.cuda.synchronize()
+    assert xs.xs_attn_get_device_error() == 0
+    del q, k, v
+    Sl = w.S // w.P
+    for p in range(w.P):
+        exp = di.layout_code_value_torch(w.B, w.S, w.H, w.D, s_offset=p * Sl, S_rows=Sl)
+        eq = outs[p].view(torch.int16) == exp.view(torch.int16)
+        assert bool(eq.all()), f"{name}: shard {p}: {int((~eq).sum())} elements differ"
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_random_sampled_rows_full(xs, name):
+    import oracle
+    w = di.WORKLOADS[name]
+    qb, kb, vb = di.random_qkv(w)
+    outs = _shards(w)
+    xs.xs_attn_a2a_fwd(bits_to_torch(qb), bits_to_torch(kb), bits_to_torch(vb), outs, w.scale)
+    torch.cuda.synchronize()
+    assert xs.xs_attn_get_device_error() == 0
+    rb, rs = di.sample_rows(w, ROWS[name])
+    ref = oracle.attention_rows(qb, kb, vb, w.scale, rb, rs)          # [n, H, D]
+    mass = oracle.attention_rows(qb, kb, abs_bits(vb), w.scale, rb, rs)
+    Sl = w.S // w.P
+    got = np.stack([torch_to_f64(outs[int(s) // Sl][int(b), int(s) % Sl]) for b, s in zip(rb, rs)])
+    assert_close(got, ref, mass, name)

@@ -66,3 +66,13 @@ def test_sample_rows_cover_shard_edges():
 def test_workload_table():
     assert di.WORKLOADS["video_large"].flops == 4 * 40 * 75776 ** 2 * 128
     assert di.SWEEP_S[0] == 1024 and di.SWEEP_S[-1] == 131072 and len(di.SWEEP_S) == 8
+
+
+def test_layout_code_torch_matches_numpy():
+    torch = pytest.importorskip("torch")
+    for (B, S, H, D) in [(2, 256, 3, 64), (1, 1000, 2, 128)]:
+        q, k, v, sc = di.layout_code_inputs(B, S, H, D)
+        tq, tk, tv, tsc = di.layout_code_inputs_torch(B, S, H, D, device="cpu")
+        assert sc == tsc
+        for a, t in ((q, tq), (k, tk), (v, tv)):
+            np.testing.assert_array_equal(a, t.view(torch.int16).numpy().view(np.uint16))
