@@ -132,6 +132,22 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a host float over all ranks (gloo); identity for one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Weak scaling: every rank processes its own copy of the workload."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def to_device(bits, torch, dev):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
@@ -258,13 +274,9 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device error status {status}")
 
-    total_ms = sum(per_step)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per_step), world)
     ms_per_step = total_ms / args.steps
-    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(w.flops, ms_per_step, world)
 
     # ablation: attention alone (contiguous store) and attention + separate re-layout
     n_abl = max(10, min(args.steps, 50))
@@ -283,11 +295,7 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(2):
         e2e_fn()
     n_e2e = max(3, min(args.steps, 20))
-    e2e_ms = statistics.mean(time_steps(torch, e2e_fn, n_e2e, flush, stream))
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(statistics.mean(time_steps(torch, e2e_fn, n_e2e, flush, stream)), world)
     if xs.xs_attn_get_device_error(stream) != 0:
         raise RuntimeError("device error after ablation / e2e runs")
 
@@ -320,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
         "overhead_pct": 100.0 * (t_fused - t_alone) / t_alone,
         "ablation": {"attention_alone_ms": t_alone, "fused_ms": t_fused, "attention_plus_relayout_ms": t_serial,
                      "serial_over_fused": t_serial / t_fused, "runs": n_abl, "statistic": "median"},
-        "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": whole_job_tflops(w.flops, e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 3 * w.tensor_bytes, "d2h_bytes_per_step": w.tensor_bytes,
                 "ms_per_step": e2e_ms, "api": "xs_attn_a2a_fwd_staged"},
         "gpu_launches": args.steps,
