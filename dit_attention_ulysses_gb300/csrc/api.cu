@@ -9,6 +9,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -107,7 +108,7 @@ int check_shape(int B, int S, int H, int D, int P, bool need_div) {
     // sizes: elements per tensor and the work-unit count must fit the kernels' index types
     const int64_t elems = static_cast<int64_t>(B) * S * H * D;
     if (elems > (int64_t(1) << 40)) return XS_ERR_SHAPE;
-    const int64_t units = static_cast<int64_t>(B) * H * ((S + 255) / 256);
+    const int64_t units = static_cast<int64_t>(B) * H * ((S + 127) / 128);
     if (units > INT32_MAX) return XS_ERR_SHAPE;
     return XS_OK;
 }
@@ -152,8 +153,19 @@ int validate_attn(const void* q, const void* k, const void* v, void* const* outs
     return check_disjoint(o, n_out, ins, 3);
 }
 
+// Limit for every wait inside the kernels.  One second by default: no single
+// wait of a healthy launch takes more than microseconds.  XSATTN_WAIT_TIMEOUT_NS
+// overrides it (a test sets 0 to make the first unfinished wait expire and
+// check that the launch reports XS_ERR_DEVICE_TIMEOUT and the context stays
+// usable).
 unsigned long long timeout_ns() {
-    return 1000000000ull;  // one second: no single wait in a healthy launch takes more than microseconds
+    const char* env = std::getenv("XSATTN_WAIT_TIMEOUT_NS");
+    if (env && *env) {
+        char* end = nullptr;
+        const unsigned long long v = std::strtoull(env, &end, 10);
+        if (end && *end == '\0') return v;
+    }
+    return 1000000000ull;
 }
 
 int run_attention(const void* q, const void* k, const void* v, const xs::EpiParams& epi, int B, int S, int H, int D,
@@ -171,8 +183,8 @@ int run_attention(const void* q, const void* k, const void* v, const xs::EpiPara
     a.S = S;
     a.H = H;
     a.n_kv = (S + 127) / 128;
-    a.n_qu = (S + 255) / 256;
-    a.units = B * H * a.n_qu;
+    a.n_qt = (S + 127) / 128;
+    a.units = B * H * a.n_qt;
     a.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.epi = epi;
     a.timeout_ns = timeout_ns();

@@ -8,32 +8,41 @@
 // P device buffers, so the "remote store" is a 16-byte vector store into the
 // owner's [B, S/P, H, D] shard.
 //
-// Kernel organisation (one persistent CTA per SM, 10 warps):
-//   warps 0-3  softmax + epilogue for Q tile 0 of the current work unit
-//   warps 4-7  softmax + epilogue for Q tile 1
-//   warp  8    TMA producer: Q tiles, then the K/V ring (K_0, V_0, K_1, V_1, ...)
-//   warp  9    tcgen05 MMA issuer (one elected lane) and TMEM owner
-// A work unit is (b, h, 256 query rows) = two 128-row Q tiles that share every
-// K/V block.  MMA order per K/V block j:  PV0_{j-1}, S0_j, PV1_{j-1}, S1_j, so
-// each tile's softmax runs while the tensor core works on the other tile.
+// Kernel organisation (one persistent CTA per SM, 11 warps):
+//   warps 0-7  softmax + epilogue of the current 128-row Q tile; two threads per
+//              row: warp w owns rows 32*(w%4) .. +31 (its TMEM lane quarter) and
+//              key columns 64*(w/4) .. +63 of every score block
+//   warp  8    TMA producer: Q tile of each work unit, then the K/V ring in
+//              consumption order K0, K1, V0, K2, V1, K3, ...  (D = 128: one Q
+//              buffer, reloaded as soon as the unit's last S MMA has read it;
+//              D = 64: two Q buffers)
+//   warp  9    issuer of the S = Q K^T MMAs (one lane) and TMEM owner
+//   warp 10    issuer of the O += P V MMAs (one lane)
+// The tcgen05 issue queue is shallow, so any control work an issuing thread
+// does between MMAs (waits, commits) leaves the tensor core idle; with two
+// issuers, one thread's control work overlaps the other thread's MMAs.
+// A work unit is (b, h, 128 query rows), numbered head-major so that the CTAs
+// running at the same time share K/V through L2.
 //
 // TMEM (512 columns x 128 lanes, fp32):
-//   [  0,128)  S0 (scores of tile 0); P0 (bf16, 2 per column) overwrites [0,64)
-//   [128,256)  S1 / P1
-//   [256,256+D) O0 accumulator,  [256+D, 256+2D) O1 accumulator
+//   [  0,128) S buffer 0    [128,256) S buffer 1        (scores, double-buffered)
+//   [256,320) P buffer 0    [320,384) P buffer 1        (bf16 P, 2 per column)
+//   [384,384+D) O accumulator
+// S(j+2) is issued as soon as the softmax has read S(j) (and K(j+2) has
+// arrived); PV(j) as soon as P(j) is written.  The tensor core computes S(j+2)
+// and PV(j) while the softmax works on block j+1, so softmax and MMAs overlap
+// completely; the softmax never waits for a PV except before reusing a P buffer
+// (PV(j-2)) and in the rare O rescale (PV(j-1)).
 //
-// Shared memory (128-byte swizzled, 1024-byte aligned):
-//   Q0, Q1 tiles [128 x D] as D/64 panels of [128 rows x 128 B]
-//   KV ring of NS stages, each one K or V block [128 x D] in the same panel form
-//   mbarriers, TMEM base address, abort flag
-//
-// Softmax (per row, one thread per row, base-2 domain with c = scale*log2(e)):
-//   m_blk = max_j s_j * c;  m_new = max(m_run, m_blk)
-//   lazy rescale: only if m_new - m_run > 8 is the running max moved (and O, l
-//   multiplied by 2^(m_run - m_new)); otherwise the stale max is kept, which
-//   bounds p by 2^8 and changes nothing after the final division by l.
-//   p_j = 2^(s_j*c - m),  l = l*alpha + sum_j p_j,  P -> bf16 into TMEM.
-// Epilogue: O / l -> bf16 -> st.global.v4 into the destination row.
+// Softmax (base 2, c = scale*log2(e) folded into one FMA, MUFU ex2):
+//   each thread takes the max of its 64 scores; the two threads of a row combine
+//   them through shared memory and a per-warp-pair mbarrier (a bounded wait);
+//   lazy rescale: the running max moves (and O, l are multiplied by
+//   2^(m_run - m_new)) only when the block max exceeds it by more than 8;
+//   p = 2^(s*c - m) -> bf16 -> TMEM P buffer; l accumulates the fp32 p.
+// Epilogue (the fused A2A): after the last PV each thread normalises its half of
+// the O row by 1/l and stores it with 16-byte st.global.v4 into the destination
+// row of the owning shard, then goes on to the next work unit.
 //
 // Every wait is bounded by a time limit; on expiry the kernel records
 // XS_ERR_DEVICE_TIMEOUT in the device error word, raises a CTA-wide abort flag,
@@ -55,12 +64,15 @@ namespace {
 
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_N = 128;
-constexpr int Q_TILES = 2;
-constexpr int UNIT_ROWS = BLOCK_M * Q_TILES;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 352;
+constexpr int NUM_SOFTMAX = 256;
 constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA_S = 9;
+constexpr int WARP_MMA_PV = 10;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL = 0;     // + 128 * buffer
+constexpr uint32_t P_COL = 256;   // + 64 * buffer
+constexpr uint32_t O_COL = 384;
 constexpr int PANEL_BYTES = BLOCK_M * 128;  // 128 rows x 64 bf16
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
 
@@ -68,314 +80,413 @@ template <int D>
 struct Cfg {
     static constexpr int TILE_BYTES = BLOCK_M * D * 2;
     static constexpr int PANELS = D / 64;
-    static constexpr int KV_STAGES = (D == 128) ? 5 : 8;
+    static constexpr int Q_BUFS = (D == 128) ? 1 : 2;
+    static constexpr int KV_STAGES = (D == 128) ? 5 : 10;
     static constexpr int Q_OFF = 0;
-    static constexpr int KV_OFF = Q_TILES * TILE_BYTES;
-    static constexpr int BAR_OFF = KV_OFF + KV_STAGES * TILE_BYTES;
+    static constexpr int KV_OFF = Q_BUFS * TILE_BYTES;
+    static constexpr int XCH_OFF = KV_OFF + KV_STAGES * TILE_BYTES;  // row max / row sum exchange
+    static constexpr int XMAX_BYTES = 2 * 2 * BLOCK_M * 4;           // [block parity][half][row] fp32
+    static constexpr int XCH_BYTES = XMAX_BYTES + 2 * BLOCK_M * 4;   // + sums [half][row]
+    static constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
     // barrier indices
-    static constexpr int B_Q_FULL = 0;                 // [2]
-    static constexpr int B_Q_FREE = 2;                 // [2]
-    static constexpr int B_S_READY = 4;                // [2]
-    static constexpr int B_P_READY = 6;                // [2]
-    static constexpr int B_O_FINAL = 8;                // [2]
-    static constexpr int B_O_FREE = 10;                // [2]
-    static constexpr int B_DRAIN = 12;                 // [1]
-    static constexpr int B_KV_FULL = 13;               // [NS]
-    static constexpr int B_KV_FREE = 13 + KV_STAGES;   // [NS]
-    static constexpr int NUM_BARS = 13 + 2 * KV_STAGES;
+    static constexpr int B_Q_FULL = 0;                 // [2]  TMA -> MMA, per Q buffer
+    static constexpr int B_Q_FREE = 2;                 // [2]  MMA -> TMA
+    static constexpr int B_S_FULL = 4;                 // [2]  MMA -> softmax, per S buffer
+    static constexpr int B_S_FREE = 6;                 // [2]  softmax -> MMA (scores read)
+    static constexpr int B_P_FULL = 8;                 // [2]  softmax -> MMA, per P buffer
+    static constexpr int B_P_FREE = 10;                // [2]  MMA -> softmax (PV done reading P)
+    static constexpr int B_O_FINAL = 12;               // [1]  MMA -> epilogue
+    static constexpr int B_O_FREE = 13;                // [1]  epilogue -> MMA
+    static constexpr int B_DRAIN = 14;                 // [1]  both issuers
+    static constexpr int B_PAIR = 15;                  // [4]  the two softmax warps of a lane quarter
+    static constexpr int B_KV_FULL = 19;               // [NS] TMA -> MMA
+    static constexpr int B_KV_FREE = 19 + KV_STAGES;   // [NS] MMA -> TMA
+    static constexpr int NUM_BARS = 19 + 2 * KV_STAGES;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-    static constexpr uint32_t O_COL = 256;
 };
 
-// Bounded wait, executed by a whole warp; the result is warp-uniform.
+// Bounded wait, executed by a whole warp; the result is warp-uniform.  The
+// first probe is a non-blocking test; after it the time limit is checked before
+// every further probe, and those probes may suspend the warp (up to 200 us each)
+// instead of spinning.  A limit of 0 therefore gives up at the first wait that
+// is not already over.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t timeout_ns) {
-    bool ok = mbar_try_wait(bar, parity);
+    bool ok = mbar_test_wait(bar, parity);
     if (!__all_sync(0xffffffffu, ok)) {
         const uint64_t t0 = globaltimer_ns();
         while (!ok) {
-            for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait(bar, parity);
-            if (ok) break;
             if (*abort_flag) break;
-            if (globaltimer_ns() - t0 > timeout_ns) {
+            if (globaltimer_ns() - t0 >= timeout_ns) {
                 *abort_flag = 1;
                 atomicCAS(&g_device_error, 0, XS_DEVICE_TIMEOUT_CODE);
                 break;
             }
+            ok = mbar_try_wait_sleep(bar, parity, 200000u);
         }
         ok = __all_sync(0xffffffffu, ok);
     }
     return ok;
 }
 
-template <int D>
-__device__ __forceinline__ void decode_unit(int u, const AttnArgs& a, int& b, int& h, int& qu) {
-    qu = u % a.n_qu;
-    const int bh = u / a.n_qu;
+// The same bounded wait for a single thread (the issuing lanes of the producer
+// and MMA roles), without warp votes.
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            uint64_t timeout_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 >= timeout_ns) {
+            *abort_flag = 1;
+            atomicCAS(&g_device_error, 0, XS_DEVICE_TIMEOUT_CODE);
+            return false;
+        }
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    }
+}
+
+// Ring position of K(j) / V(j) within a unit of n key blocks (consumption order
+// K0, K1, V0, K2, V1, K3, ..., V(n-3), K(n-1), V(n-2), V(n-1)).
+__device__ __forceinline__ uint32_t ring_pos_k(int j) { return j < 2 ? j : 2 * j - 1; }
+__device__ __forceinline__ uint32_t ring_pos_v(int j, int n) { return (j + 2 < n) ? 2 * j + 2 : n + j; }
+
+__device__ __forceinline__ void decode_unit(int u, const AttnArgs& a, int& b, int& h, int& qt) {
+    qt = u % a.n_qt;
+    const int bh = u / a.n_qt;
     h = bh % a.H;
     b = bh / a.H;
 }
 
+// Ring item `i` of a unit with n key blocks, in the consumption order
+// K0, K1, V0, K2, V1, K3, ..., V(n-3), K(n-1), V(n-2), V(n-1): the block index
+// and whether it is a V block.
+__device__ __forceinline__ void ring_item(int i, int n, int& blk, bool& is_v) {
+    if (n == 1) {
+        blk = 0;
+        is_v = (i == 1);
+        return;
+    }
+    if (i < 2) {
+        blk = i;
+        is_v = false;
+        return;
+    }
+    const int r = i - 2;  // pairs (V_j, K_{j+2}) for j + 2 < n, then V(n-2), V(n-1)
+    const int pairs = n - 2;
+    if (r < 2 * pairs) {
+        is_v = (r & 1) == 0;
+        blk = is_v ? (r >> 1) : (r >> 1) + 2;
+    } else {
+        is_v = true;
+        blk = n - 2 + (r - 2 * pairs);
+    }
+}
+
 // ---------------------------------------------------------------- producer
+// Run by one thread.
 template <int D>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               const AttnArgs& a, uint8_t* smem, uint32_t bar0, volatile int* abort_flag) {
     using C = Cfg<D>;
-    const bool leader = lane_id() == 0;
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
-    uint32_t item = 0;
+    uint32_t item = 0;        // ring items issued over the CTA's lifetime
     int u_iter = 0;
+    int q_last = -1;          // u_iter of the last Q load issued
     bool ok = true;
+    const int n = a.n_kv;
     for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++u_iter) {
-        int b, h, qu;
-        decode_unit<D>(u, a, b, h, qu);
-        for (int t = 0; t < Q_TILES && ok; ++t) {
-            if (u_iter > 0) ok = warp_wait(bar(C::B_Q_FREE + t), (u_iter - 1) & 1, abort_flag, a.timeout_ns);
+        int b, h, qt;
+        decode_unit(u, a, b, h, qt);
+        const int qb = u_iter % C::Q_BUFS;
+        if (u_iter >= C::Q_BUFS)
+            ok = thread_wait(bar(C::B_Q_FREE + qb), ((u_iter / C::Q_BUFS) - 1) & 1, abort_flag, a.timeout_ns);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(C::B_Q_FULL + qb), C::TILE_BYTES);
+        for (int pnl = 0; pnl < C::PANELS; ++pnl)
+            tma_load_4d(sbase + C::Q_OFF + qb * C::TILE_BYTES + pnl * PANEL_BYTES, tq, bar(C::B_Q_FULL + qb),
+                        pnl * 64, h, qt * BLOCK_M, b);
+        q_last = u_iter;
+        for (int i = 0; i < 2 * n && ok; ++i) {
+            int blk;
+            bool is_v;
+            ring_item(i, n, blk, is_v);
+            const uint32_t stage = item % C::KV_STAGES;
+            const uint32_t round = item / C::KV_STAGES;
+            if (round > 0) ok = thread_wait(bar(C::B_KV_FREE + stage), (round - 1) & 1, abort_flag, a.timeout_ns);
             if (!ok) break;
-            if (leader) {
-                int s0 = qu * UNIT_ROWS + t * BLOCK_M;
-                if (s0 >= a.S) s0 = 0;  // tile entirely past the end: load any in-bounds rows, never stored
-                mbar_arrive_expect_tx(bar(C::B_Q_FULL + t), C::TILE_BYTES);
-                for (int pnl = 0; pnl < C::PANELS; ++pnl)
-                    tma_load_4d(sbase + C::Q_OFF + t * C::TILE_BYTES + pnl * PANEL_BYTES, tq,
-                                bar(C::B_Q_FULL + t), pnl * 64, h, s0, b);
-            }
-            __syncwarp();
-        }
-        for (int j = 0; j < a.n_kv && ok; ++j) {
-            for (int kv = 0; kv < 2 && ok; ++kv, ++item) {
-                const uint32_t stage = item % C::KV_STAGES;
-                const uint32_t round = item / C::KV_STAGES;
-                if (round > 0) ok = warp_wait(bar(C::B_KV_FREE + stage), (round - 1) & 1, abort_flag, a.timeout_ns);
-                if (!ok) break;
-                if (leader) {
-                    mbar_arrive_expect_tx(bar(C::B_KV_FULL + stage), C::TILE_BYTES);
-                    for (int pnl = 0; pnl < C::PANELS; ++pnl)
-                        tma_load_4d(sbase + C::KV_OFF + stage * C::TILE_BYTES + pnl * PANEL_BYTES,
-                                    kv ? tv : tk, bar(C::B_KV_FULL + stage), pnl * 64, h, j * BLOCK_N, b);
-                }
-                __syncwarp();
-            }
+            mbar_arrive_expect_tx(bar(C::B_KV_FULL + stage), C::TILE_BYTES);
+            for (int pnl = 0; pnl < C::PANELS; ++pnl)
+                tma_load_4d(sbase + C::KV_OFF + stage * C::TILE_BYTES + pnl * PANEL_BYTES, is_v ? tv : tk,
+                            bar(C::B_KV_FULL + stage), pnl * 64, h, blk * BLOCK_N, b);
+            ++item;
         }
     }
     if (!ok) {
         // Let the copies already issued land before the CTA exits: wait (bounded)
-        // for the newest phase of every ring stage that was used.
+        // for the newest phase of every ring stage used and for the last Q load.
         volatile int no_abort = 0;
         for (uint32_t back = 1; back <= C::KV_STAGES && back <= item; ++back) {
             const uint32_t it = item - back;
-            warp_wait(bar(C::B_KV_FULL + it % C::KV_STAGES), (it / C::KV_STAGES) & 1, &no_abort, 20000000ull);
+            thread_wait(bar(C::B_KV_FULL + it % C::KV_STAGES), (it / C::KV_STAGES) & 1, &no_abort, 20000000ull);
         }
+        if (q_last >= 0)
+            thread_wait(bar(C::B_Q_FULL + q_last % C::Q_BUFS), (q_last / C::Q_BUFS) & 1, &no_abort, 20000000ull);
     }
 }
 
 // --------------------------------------------------------------------- MMA
+// Q / K operand (K-major, 128-B swizzle): k-step kk covers 16 columns of D.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
+    return smem_desc_sw128(tile_addr + (kk >> 2) * PANEL_BYTES + (kk & 3) * 32, 16, 1024);
+}
+// V operand (MN-major = D contiguous, 128-B swizzle): k-step kk covers 16 keys;
+// 8-key groups are 1024 B apart (SBO), 64-wide D panels PANEL_BYTES apart (LBO).
+__device__ __forceinline__ uint64_t vmajor_desc(uint32_t tile_addr, int kk) {
+    return smem_desc_sw128(tile_addr + kk * 2048, PANEL_BYTES, 1024);
+}
+
+// Issuer of S(j) = Q K_j^T (SS) into S buffer (block index) & 1.  One thread.
 template <int D>
-__device__ void mma_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
-                         volatile int* abort_flag) {
+__device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
+                           volatile int* abort_flag) {
     using C = Cfg<D>;
-    const bool leader = lane_id() == 0;
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
     constexpr uint32_t IDESC_QK = idesc_bf16_f32(BLOCK_M, BLOCK_N, 0);
-    constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 1);
-
-    // Q / K operand (K-major, 128-B swizzle): k-step kk covers 16 columns of D.
-    auto kmajor_desc = [&](uint32_t tile_addr, int kk) {
-        return smem_desc_sw128(tile_addr + (kk >> 2) * PANEL_BYTES + (kk & 3) * 32, 16, 1024);
-    };
-    // V operand (MN-major = D contiguous, 128-B swizzle): k-step kk covers 16 keys;
-    // 8-key groups are 1024 B apart (SBO), 64-wide D panels PANEL_BYTES apart (LBO).
-    auto vdesc = [&](uint32_t tile_addr, int kk) {
-        return smem_desc_sw128(tile_addr + kk * 2048, PANEL_BYTES, 1024);
-    };
-    auto s_tmem = [&](int t) { return tmem_base + static_cast<uint32_t>(t) * 128u; };
-    auto o_tmem = [&](int t) { return tmem_base + C::O_COL + static_cast<uint32_t>(t) * D; };
-
-    uint32_t item = 0;
-    uint32_t p_count[2] = {0, 0};
+    const int n = a.n_kv;
+    uint32_t g = 0;      // key blocks over the CTA's lifetime
     int u_iter = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++u_iter) {
-        const int n = a.n_kv;
-        for (int t = 0; t < Q_TILES && ok; ++t)
-            ok = warp_wait(bar(C::B_Q_FULL + t), u_iter & 1, abort_flag, a.timeout_ns);
-        if (!ok) break;
-        // K_0 -> S_t_0 for both tiles
-        uint32_t k_stage = item % C::KV_STAGES;
-        ok = warp_wait(bar(C::B_KV_FULL + k_stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns);
-        if (!ok) break;
-        ++item;
-        tc_fence_after();
-        if (leader) {
-            const uint32_t kaddr = sbase + C::KV_OFF + k_stage * C::TILE_BYTES;
-            for (int t = 0; t < Q_TILES; ++t) {
-                const uint32_t qaddr = sbase + C::Q_OFF + t * C::TILE_BYTES;
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(s_tmem(t), kmajor_desc(qaddr, kk), kmajor_desc(kaddr, kk), IDESC_QK, kk > 0);
-                mma_commit(bar(C::B_S_READY + t));
-                if (n == 1) mma_commit(bar(C::B_Q_FREE + t));
-            }
-            mma_commit(bar(C::B_KV_FREE + k_stage));
-        }
-        __syncwarp();
+        const int qb = u_iter % C::Q_BUFS;
+        const uint32_t qaddr = sbase + C::Q_OFF + qb * C::TILE_BYTES;
+        const uint32_t item0 = static_cast<uint32_t>(u_iter) * 2u * n;
+        ok = thread_wait(bar(C::B_Q_FULL + qb), (u_iter / C::Q_BUFS) & 1, abort_flag, a.timeout_ns);
         for (int j = 0; j < n && ok; ++j) {
-            const uint32_t v_stage = item % C::KV_STAGES;
-            ok = warp_wait(bar(C::B_KV_FULL + v_stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns);
+            const uint32_t gs = g + j;
+            const uint32_t sb = gs & 1;
+            // the softmax has read this S buffer's previous scores (block gs-2)
+            if (gs >= 2) ok = thread_wait(bar(C::B_S_FREE + sb), ((gs >> 1) - 1) & 1, abort_flag, a.timeout_ns);
+            const uint32_t item = item0 + ring_pos_k(j);
+            const uint32_t stage = item % C::KV_STAGES;
+            if (ok) ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns);
             if (!ok) break;
-            ++item;
-            const bool has_next = (j + 1) < n;
-            k_stage = item % C::KV_STAGES;
-            const uint32_t k_round = item / C::KV_STAGES;
-            if (has_next) ++item;
-            for (int t = 0; t < Q_TILES && ok; ++t) {
-                ok = warp_wait(bar(C::B_P_READY + t), p_count[t] & 1, abort_flag, a.timeout_ns);
-                ++p_count[t];
-                if (ok && j == 0 && u_iter > 0)
-                    ok = warp_wait(bar(C::B_O_FREE + t), (u_iter - 1) & 1, abort_flag, a.timeout_ns);
-                if (!ok) break;
-                tc_fence_after();
-                if (leader) {
-                    const uint32_t vaddr = sbase + C::KV_OFF + v_stage * C::TILE_BYTES;
-                    for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-                        mma_ts(o_tmem(t), s_tmem(t) + kk * 8, vdesc(vaddr, kk), IDESC_PV, (j > 0) || (kk > 0));
-                    if (j == n - 1) mma_commit(bar(C::B_O_FINAL + t));
-                    if (t == Q_TILES - 1) mma_commit(bar(C::B_KV_FREE + v_stage));
-                }
-                __syncwarp();
-                if (has_next) {
-                    if (t == 0) {
-                        ok = warp_wait(bar(C::B_KV_FULL + k_stage), k_round & 1, abort_flag, a.timeout_ns);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    if (leader) {
-                        const uint32_t kaddr = sbase + C::KV_OFF + k_stage * C::TILE_BYTES;
-                        const uint32_t qaddr = sbase + C::Q_OFF + t * C::TILE_BYTES;
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss(s_tmem(t), kmajor_desc(qaddr, kk), kmajor_desc(kaddr, kk), IDESC_QK, kk > 0);
-                        mma_commit(bar(C::B_S_READY + t));
-                        if (j + 1 == n - 1) mma_commit(bar(C::B_Q_FREE + t));
-                        if (t == Q_TILES - 1) mma_commit(bar(C::B_KV_FREE + k_stage));
-                    }
-                    __syncwarp();
-                }
-            }
+            tc_fence_after();
+            const uint32_t kaddr = sbase + C::KV_OFF + stage * C::TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tmem_base + S_COL + sb * 128u, kmajor_desc(qaddr, kk), kmajor_desc(kaddr, kk), IDESC_QK, kk > 0);
+            mma_commit(bar(C::B_S_FULL + sb));
+            mma_commit(bar(C::B_KV_FREE + stage));
+            if (j == n - 1) mma_commit(bar(C::B_Q_FREE + qb));
         }
+        g += n;
     }
-    // Drain: every MMA this warp issued has completed once B_DRAIN flips.
-    if (leader) mma_commit(bar(C::B_DRAIN));
-    __syncwarp();
+    // Drain: B_DRAIN completes when both issuers' MMAs have all completed.
+    mma_commit(bar(C::B_DRAIN));
     volatile int no_abort = 0;
-    warp_wait(bar(C::B_DRAIN), 0, &no_abort, ok ? a.timeout_ns : 20000000ull);
+    thread_wait(bar(C::B_DRAIN), 0, &no_abort, ok ? a.timeout_ns : 20000000ull);
+}
+
+// Issuer of PV(j): O += P(j) V_j (A = P buffer from TMEM).  One thread.
+template <int D>
+__device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
+                            volatile int* abort_flag) {
+    using C = Cfg<D>;
+    const uint32_t sbase = smem_addr(smem);
+    auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
+    constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 1);
+    const int n = a.n_kv;
+    uint32_t g = 0;
+    int u_iter = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++u_iter) {
+        const uint32_t item0 = static_cast<uint32_t>(u_iter) * 2u * n;
+        for (int j = 0; j < n && ok; ++j) {
+            const uint32_t gj = g + j;
+            const uint32_t pb = gj & 1;
+            ok = thread_wait(bar(C::B_P_FULL + pb), (gj >> 1) & 1, abort_flag, a.timeout_ns);
+            // the epilogue has read the previous unit's O (PV(0) overwrites it)
+            if (ok && j == 0 && u_iter > 0) ok = thread_wait(bar(C::B_O_FREE), (u_iter - 1) & 1, abort_flag, a.timeout_ns);
+            const uint32_t item = item0 + ring_pos_v(j, n);
+            const uint32_t stage = item % C::KV_STAGES;
+            if (ok) ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vaddr = sbase + C::KV_OFF + stage * C::TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+                mma_ts(tmem_base + O_COL, tmem_base + P_COL + pb * 64u + kk * 8, vmajor_desc(vaddr, kk), IDESC_PV,
+                       (j > 0) || (kk > 0));
+            mma_commit(bar(C::B_P_FREE + pb));
+            mma_commit(bar(C::B_KV_FREE + stage));
+            if (j == n - 1) mma_commit(bar(C::B_O_FINAL));
+        }
+        g += n;
+    }
+    mma_commit(bar(C::B_DRAIN));
+    volatile int no_abort = 0;
+    thread_wait(bar(C::B_DRAIN), 0, &no_abort, ok ? a.timeout_ns : 20000000ull);
 }
 
 // ------------------------------------------------------- softmax + epilogue
+// Maximum of a thread's 64 scores: four independent 3-input chains.
+__device__ __forceinline__ float max64(const uint32_t (&sr)[2][32]) {
+    float mx[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) mx[r] = __uint_as_float(sr[r >> 1][(r & 1) * 16]);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+            const int r = q * 2 + (i >> 4);
+            mx[r] = fmax3(mx[r], __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]));
+            mx[r] = fmax3(mx[r], __uint_as_float(sr[q][i + 2]), __uint_as_float(sr[q][i + 3]));
+        }
+    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// p = 2^(s*c - m) for a thread's 64 scores: one FMA and one MUFU ex2 each,
+// packed to bf16 pairs; the fp32 values are summed in four independent chains.
+// TAIL: columns at or past `valid` (keys past the sequence) get p = 0.
+template <bool TAIL>
+__device__ __forceinline__ float exp64(const uint32_t (&sr)[2][32], float c, float m, int col0, int valid,
+                                       uint32_t (&pk)[32]) {
+    const float neg_m = -m;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int q = i >> 4;
+        const int e = (i & 15) * 2;
+        float p0 = ex2_approx(fmaf(__uint_as_float(sr[q][e]), c, neg_m));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sr[q][e + 1]), c, neg_m));
+        if (TAIL) {
+            const int col = col0 + q * 32 + e;
+            if (col >= valid) p0 = 0.0f;
+            if (col + 1 >= valid) p1 = 0.0f;
+        }
+        acc[i & 3] += p0 + p1;
+        pk[i] = pack_bf16x2(p0, p1);
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 template <int D>
-__device__ void softmax_role(const AttnArgs& a, uint32_t bar0, uint32_t tmem_base, volatile int* abort_flag) {
+__device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
+                             volatile int* abort_flag) {
     using C = Cfg<D>;
+    constexpr int DH = D / 2;  // O columns owned by each of a row's two threads
     const int warp = threadIdx.x >> 5;
-    const int t = warp >> 2;                  // Q tile of this warpgroup
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int half = warp >> 2;               // key columns [64*half, 64*half + 64)
     const int row = quarter * 32 + static_cast<int>(lane_id());
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_t = tmem_base + lane_off + static_cast<uint32_t>(t) * 128u;
-    const uint32_t o_t = tmem_base + lane_off + C::O_COL + static_cast<uint32_t>(t) * D;
+    const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    float* xmax = reinterpret_cast<float*>(smem + C::XCH_OFF);                   // [2][2][128]
+    float* xsum = reinterpret_cast<float*>(smem + C::XCH_OFF + C::XMAX_BYTES);  // [2][128]
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
     const float c = a.c;
+    const int n = a.n_kv;
+    // Exchange with the other thread of this row (the warp 4 apart): both
+    // threads have stored their value to shared memory before either reads.
+    uint32_t xchg = 0;
+    auto pair_exchange = [&]() -> bool {
+        mbar_arrive(bar(C::B_PAIR + quarter));
+        return warp_wait(bar(C::B_PAIR + quarter), (xchg++) & 1, abort_flag, a.timeout_ns);
+    };
 
-    uint32_t s_count = 0;
+    uint32_t g = 0;
     int u_iter = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++u_iter) {
-        int b, h, qu;
-        decode_unit<D>(u, a, b, h, qu);
+        int b, h, qt;
+        decode_unit(u, a, b, h, qt);
         float m_run = 0.0f, l_run = 0.0f;
-        for (int j = 0; j < a.n_kv; ++j) {
-            ok = warp_wait(bar(C::B_S_READY + t), s_count & 1, abort_flag, a.timeout_ns);
-            ++s_count;
+        for (int j = 0; j < n; ++j, ++g) {
+            const uint32_t sb = g & 1;
+            ok = warp_wait(bar(C::B_S_FULL + sb), (g >> 1) & 1, abort_flag, a.timeout_ns);
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(s_t + q * 32, sr[q]);
+            uint32_t sr[2][32];
+            tmem_ld32(t_base + S_COL + sb * 128u + half * 64, sr[0]);
+            tmem_ld32(t_base + S_COL + sb * 128u + half * 64 + 32, sr[1]);
             tmem_wait_ld();
-            const int valid = a.S - j * BLOCK_N;  // keys of this block inside the sequence
+            tc_fence_before();
+            mbar_arrive(bar(C::B_S_FREE + sb));  // the MMA may now overwrite this S buffer
+            const int valid = a.S - j * BLOCK_N;
             const bool tail = valid < BLOCK_N;
             if (tail) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int q = 0; q < 2; ++q)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (q * 32 + i >= valid) sr[q][i] = 0xff800000u;  // -inf
+                        if (half * 64 + q * 32 + i >= valid) sr[q][i] = 0xff800000u;  // -inf
             }
-            float mx = __uint_as_float(sr[0][0]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[q][i]));
-            const float m_blk = mx * c;
+            // row max: combine the two halves of the row (slots alternate by block
+            // parity, so a fast thread never overwrites a value still to be read)
+            float* xm = xmax + (g & 1) * 2 * BLOCK_M;
+            xm[half * BLOCK_M + row] = max64(sr);
+            ok = pair_exchange();
+            if (!ok) break;
+            const float m_blk = fmaxf(xm[row], xm[BLOCK_M + row]) * c;
             float m_use, alpha = 1.0f;
             bool rescale = false;
             if (j == 0) {
                 m_use = m_blk;
+            } else if (m_blk - m_run > RESCALE_THRESHOLD) {
+                m_use = m_blk;
+                alpha = ex2_approx(m_run - m_blk);
+                rescale = true;
             } else {
-                const float m_new = fmaxf(m_run, m_blk);
-                if (m_new - m_run > RESCALE_THRESHOLD) {
-                    m_use = m_new;
-                    alpha = ex2_approx(m_run - m_new);
-                    rescale = true;
-                } else {
-                    m_use = m_run;
-                }
+                m_use = m_run;
             }
-            const float neg_m = -m_use;
-            float sum = 0.0f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int q = half * 2 + (i >> 4);
-                    const int e = (i & 15) * 2;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[q][e]), c, neg_m));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sr[q][e + 1]), c, neg_m));
-                    if (tail) {
-                        const int col = q * 32 + e;
-                        if (col >= valid) p0 = 0.0f;
-                        if (col + 1 >= valid) p1 = 0.0f;
-                    }
-                    sum += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(s_t + half * 32, pk);
-            }
+            // Lazy rescale of this thread's half of the O row (rare); PV(g-1)
+            // must have completed first.  Warp-uniform: TMEM access is collective.
             if (__any_sync(0xffffffffu, rescale)) {
+                ok = warp_wait(bar(C::B_P_FREE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag, a.timeout_ns);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
+                for (int q = 0; q < DH / 32; ++q) {
                     uint32_t orr[32];
-                    tmem_ld32(o_t + q * 32, orr);
+                    tmem_ld32(t_base + O_COL + half * DH + q * 32, orr);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-                    tmem_st32(o_t + q * 32, orr);
+                    tmem_st32(t_base + O_COL + half * DH + q * 32, orr);
                 }
             }
-            l_run = l_run * alpha + sum;
-            m_run = m_use;
+            uint32_t pk[32];
+            const float sum = tail ? exp64<true>(sr, c, m_use, half * 64, valid, pk)
+                                   : exp64<false>(sr, c, m_use, half * 64, valid, pk);
+            // P buffer sb is free once PV(g-2) has completed.
+            if (g >= 2) {
+                ok = warp_wait(bar(C::B_P_FREE + sb), ((g >> 1) - 1) & 1, abort_flag, a.timeout_ns);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            tmem_st32(t_base + P_COL + sb * 64u + half * 32, pk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_P_READY + t));
+            mbar_arrive(bar(C::B_P_FULL + sb));
+            l_run = l_run * alpha + sum;
+            m_run = m_use;
         }
         if (!ok) break;
         // ---- epilogue: the owner of this tile stores it to the destination shard
-        ok = warp_wait(bar(C::B_O_FINAL + t), u_iter & 1, abort_flag, a.timeout_ns);
+        // (one slot suffices: before a thread writes it again, both threads of the
+        // row have passed the next block's max exchange, i.e. read this value)
+        xsum[half * BLOCK_M + row] = l_run;
+        ok = pair_exchange();
+        if (!ok) break;
+        const float l_row = xsum[row] + xsum[BLOCK_M + row];
+        ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns);
         if (!ok) break;
         tc_fence_after();
-        const int s_row = qu * UNIT_ROWS + t * BLOCK_M + row;
+        const int s_row = qt * BLOCK_M + row;
         const bool store = s_row < a.S;
         __nv_bfloat16* dst = nullptr;
         if (store) {
@@ -383,13 +494,13 @@ __device__ void softmax_role(const AttnArgs& a, uint32_t bar0, uint32_t tmem_bas
             const int s_dst = s_row % a.epi.Sl;
             const int h_dst = h % a.epi.Hl;
             dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
-                  ((static_cast<size_t>(b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D;
+                  ((static_cast<size_t>(b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D + half * DH;
         }
-        const float inv_l = 1.0f / l_run;
+        const float inv_l = 1.0f / l_row;
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
+        for (int q = 0; q < DH / 32; ++q) {
             uint32_t orr[32];
-            tmem_ld32(o_t + q * 32, orr);
+            tmem_ld32(t_base + O_COL + half * DH + q * 32, orr);
             tmem_wait_ld();
             uint32_t w[16];
 #pragma unroll
@@ -402,7 +513,7 @@ __device__ void softmax_role(const AttnArgs& a, uint32_t bar0, uint32_t tmem_bas
             }
         }
         tc_fence_before();
-        mbar_arrive(bar(C::B_O_FREE + t));
+        mbar_arrive(bar(C::B_O_FREE));
     }
 }
 
@@ -419,15 +530,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
-        for (int t = 0; t < Q_TILES; ++t) {
-            mbar_init(bar0 + 8 * (C::B_Q_FULL + t), 1);
-            mbar_init(bar0 + 8 * (C::B_Q_FREE + t), 1);
-            mbar_init(bar0 + 8 * (C::B_S_READY + t), 1);
-            mbar_init(bar0 + 8 * (C::B_P_READY + t), 128);
-            mbar_init(bar0 + 8 * (C::B_O_FINAL + t), 1);
-            mbar_init(bar0 + 8 * (C::B_O_FREE + t), 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar0 + 8 * (C::B_Q_FULL + i), 1);   // (index 1 unused when Q_BUFS == 1)
+            mbar_init(bar0 + 8 * (C::B_Q_FREE + i), 1);
+            mbar_init(bar0 + 8 * (C::B_S_FULL + i), 1);
+            mbar_init(bar0 + 8 * (C::B_S_FREE + i), NUM_SOFTMAX);
+            mbar_init(bar0 + 8 * (C::B_P_FULL + i), NUM_SOFTMAX);
+            mbar_init(bar0 + 8 * (C::B_P_FREE + i), 1);
         }
-        mbar_init(bar0 + 8 * C::B_DRAIN, 1);
+        mbar_init(bar0 + 8 * C::B_O_FINAL, 1);
+        mbar_init(bar0 + 8 * C::B_O_FREE, NUM_SOFTMAX);
+        mbar_init(bar0 + 8 * C::B_DRAIN, 2);
+        for (int q = 0; q < 4; ++q) mbar_init(bar0 + 8 * (C::B_PAIR + q), 64);
         for (int s = 0; s < C::KV_STAGES; ++s) {
             mbar_init(bar0 + 8 * (C::B_KV_FULL + s), 1);
             mbar_init(bar0 + 8 * (C::B_KV_FREE + s), 1);
@@ -440,7 +554,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
     }
-    if (warp == WARP_MMA) {
+    if (warp == WARP_MMA_S) {
         tmem_alloc(smem_addr(tmem_holder), TMEM_COLS);
         tmem_relinquish();
     }
@@ -450,17 +564,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < 8) {
-        softmax_role<D>(args, bar0, tmem_base, abort_flag);
-    } else if (warp == WARP_TMA) {
-        producer_role<D>(&tmap_q, &tmap_k, &tmap_v, args, smem, bar0, abort_flag);
-    } else {
-        mma_role<D>(args, smem, bar0, tmem_base, abort_flag);
+        softmax_role<D>(args, smem, bar0, tmem_base, abort_flag);
+    } else if (lane_id() == 0) {
+        // single-thread roles; the other lanes of these warps wait at the end
+        if (warp == WARP_TMA)
+            producer_role<D>(&tmap_q, &tmap_k, &tmap_v, args, smem, bar0, abort_flag);
+        else if (warp == WARP_MMA_S)
+            mma_s_role<D>(args, smem, bar0, tmem_base, abort_flag);
+        else
+            mma_pv_role<D>(args, smem, bar0, tmem_base, abort_flag);
     }
+    __syncwarp();
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == WARP_MMA) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == WARP_MMA_S) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
 }  // namespace
@@ -469,6 +588,9 @@ template <int D>
 int attn_smem_bytes() {
     return Cfg<D>::SMEM_ALLOC;
 }
+
+static_assert(Cfg<128>::SMEM_ALLOC <= 232448, "shared memory budget (D = 128)");
+static_assert(Cfg<64>::SMEM_ALLOC <= 232448, "shared memory budget (D = 64)");
 
 template <int D>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& args,

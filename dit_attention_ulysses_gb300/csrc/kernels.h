@@ -26,8 +26,8 @@ struct EpiParams {
 struct AttnArgs {
     int B, S, H;
     int n_kv;       // ceil(S / 128) key blocks
-    int n_qu;       // ceil(S / 256) work units per (b, h)
-    int units;      // B * H * n_qu
+    int n_qt;       // ceil(S / 128) query tiles (work units) per (b, h)
+    int units;      // B * H * n_qt
     float c;        // scale * log2(e)
     EpiParams epi;
     unsigned long long timeout_ns;  // limit for every wait inside the kernel

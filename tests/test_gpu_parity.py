@@ -199,3 +199,39 @@ def test_non_default_stream(xs):
     torch.cuda.synchronize()
     for a, b in zip(ref, outs):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def _scaled_keys_case(xs, key_rows, factor, S=512, H=2, D=128, P=2, seed=11):
+    """Random inputs with a block of key rows scaled up, so that a later key block
+    holds scores far above the running max (exercises the rescale paths)."""
+    w = di.Workload("sk", B=1, H=H, S=S, D=D, P=P, scale=1 / math.sqrt(D), seed=seed)
+    q, k, v = di.random_qkv(w)
+    kf = di.bf16_bits_to_f32(k)
+    kf[:, key_rows] *= factor
+    k = di.f32_to_bf16_bits(kf)
+    ref, mass = _oracle_shards(q, k, v, w.scale, P)
+    got = np.stack([torch_to_f64(o) for o in _run_fused(xs, q, k, v, w.scale, P)])
+    assert_close(got, ref, mass, f"scaled keys {key_rows} x{factor}")
+
+
+def test_lazy_rescale_path(xs):
+    # first half of key block 1 scaled x4: its max exceeds the running max by > 8 (log2)
+    _scaled_keys_case(xs, slice(128, 192), 4.0)
+
+
+def test_speculation_fallback_path(xs):
+    # second half of key block 1 scaled x16: exceeds the speculative max by > 32 (log2)
+    _scaled_keys_case(xs, slice(192, 256), 16.0)
+
+
+def test_growing_scores_every_block(xs):
+    # every key block scaled a little more than the one before
+    w = di.Workload("grow", B=1, H=2, S=1024, D=128, P=2, scale=1 / math.sqrt(128), seed=5)
+    q, k, v = di.random_qkv(w)
+    kf = di.bf16_bits_to_f32(k)
+    for blk in range(8):
+        kf[:, blk * 128:(blk + 1) * 128] *= 1.0 + 1.5 * blk
+    k = di.f32_to_bf16_bits(kf)
+    ref, mass = _oracle_shards(q, k, v, w.scale, 2)
+    got = np.stack([torch_to_f64(o) for o in _run_fused(xs, q, k, v, w.scale, 2)])
+    assert_close(got, ref, mass, "growing")
