@@ -171,12 +171,18 @@ def cpu_oracle_sample(w, seconds_target=12.0, max_rows=None):
     q, k, v = di.random_qkv(w)
     threads = oracle.threads_used()
     per_pair = 4.0 * w.S * w.D  # flops per (row, head)
-    # calibrate on a few rows, then size the sample for ~seconds_target
-    rb, rs = di.sample_rows(w, 8, seed=5)
-    t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.scale, rb, rs)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    rate = len(rb) * w.H * per_pair / dt
+    # calibrate on a sample large enough to occupy every thread for a while
+    # (at least ~1 s), then size the timed sample for ~seconds_target
+    n_cal, dt = 8 * threads, 0.0
+    while True:
+        rb, rs = di.sample_rows(w, n_cal, seed=5)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.scale, rb, rs)
+        dt = time.perf_counter() - t0
+        if dt >= 1.0 or len(rb) >= w.B * w.S:
+            break
+        n_cal *= 4
+    rate = len(rb) * w.H * per_pair / max(dt, 1e-4)
     n = int(seconds_target * rate / (w.H * per_pair))
     n = max(8, min(n, w.B * w.S if max_rows is None else max_rows))
     rb, rs = di.sample_rows(w, n, seed=6)
@@ -278,14 +284,18 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(w.flops, ms_per_step, world)
 
-    # ablation: attention alone (contiguous store) and attention + separate re-layout
+    # ablation: attention alone (contiguous store), fused, and attention + separate
+    # re-layout, interleaved run by run so that clock drift affects all three alike
     n_abl = max(10, min(args.steps, 50))
     for fn in (alone, serial_path):
         for _ in range(3):
             fn()
-    t_alone = statistics.median(time_steps(torch, alone, n_abl, flush, stream))
-    t_fused = statistics.median(time_steps(torch, fused, n_abl, flush, stream))
-    t_serial = statistics.median(time_steps(torch, serial_path, n_abl, flush, stream))
+    ta, tf, ts = [], [], []
+    for _ in range(n_abl):
+        ta += time_steps(torch, alone, 1, flush, stream)
+        tf += time_steps(torch, fused, 1, flush, stream)
+        ts += time_steps(torch, serial_path, 1, flush, stream)
+    t_alone, t_fused, t_serial = statistics.median(ta), statistics.median(tf), statistics.median(ts)
 
     # end to end through the host-buffer entry point: H2D of q, k, v, kernel, D2H of the shards
     pin = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -327,7 +337,8 @@ def run_ours(args, rank, world, local_rank):
                      "algorithmic_bytes": 4 * w.tensor_bytes},
         "overhead_pct": 100.0 * (t_fused - t_alone) / t_alone,
         "ablation": {"attention_alone_ms": t_alone, "fused_ms": t_fused, "attention_plus_relayout_ms": t_serial,
-                     "serial_over_fused": t_serial / t_fused, "runs": n_abl, "statistic": "median"},
+                     "serial_over_fused": t_serial / t_fused, "runs": n_abl, "statistic": "median",
+                     "order": "interleaved alone/fused/serial, L2 flushed before each"},
         "e2e": {"value": whole_job_tflops(w.flops, e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 3 * w.tensor_bytes, "d2h_bytes_per_step": w.tensor_bytes,
                 "ms_per_step": e2e_ms, "api": "xs_attn_a2a_fwd_staged"},

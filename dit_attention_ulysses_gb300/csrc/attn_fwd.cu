@@ -65,7 +65,7 @@ namespace {
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_N = 128;
 constexpr int NUM_THREADS = 352;
-constexpr int NUM_SOFTMAX = 256;
+constexpr int NUM_SOFTMAX_WARPS = 8;
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA_S = 9;
 constexpr int WARP_MMA_PV = 10;
@@ -152,6 +152,14 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volat
 // K0, K1, V0, K2, V1, K3, ..., V(n-3), K(n-1), V(n-2), V(n-1)).
 __device__ __forceinline__ uint32_t ring_pos_k(int j) { return j < 2 ? j : 2 * j - 1; }
 __device__ __forceinline__ uint32_t ring_pos_v(int j, int n) { return (j + 2 < n) ? 2 * j + 2 : n + j; }
+
+// One arrival for a whole warp: every lane has finished its part (its own
+// fences included) once __syncwarp returns; lane 0 then arrives.  Replaces 32
+// arrivals on the same shared-memory word, which serialise.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive(bar);
+}
 
 __device__ __forceinline__ void decode_unit(int u, const AttnArgs& a, int& b, int& h, int& qt) {
     qt = u % a.n_qt;
@@ -393,8 +401,9 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
     // Exchange with the other thread of this row (the warp 4 apart): both
     // threads have stored their value to shared memory before either reads.
     uint32_t xchg = 0;
+    auto xslot = [&]() { return xmax + (xchg & 1) * 2 * BLOCK_M; };
     auto pair_exchange = [&]() -> bool {
-        mbar_arrive(bar(C::B_PAIR + quarter));
+        warp_arrive(bar(C::B_PAIR + quarter));
         return warp_wait(bar(C::B_PAIR + quarter), (xchg++) & 1, abort_flag, a.timeout_ns);
     };
 
@@ -415,7 +424,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
             tmem_ld32(t_base + S_COL + sb * 128u + half * 64 + 32, sr[1]);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(bar(C::B_S_FREE + sb));  // the MMA may now overwrite this S buffer
+            warp_arrive(bar(C::B_S_FREE + sb));  // the MMA may now overwrite this S buffer
             const int valid = a.S - j * BLOCK_N;
             const bool tail = valid < BLOCK_N;
             if (tail) {
@@ -425,9 +434,11 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
                     for (int i = 0; i < 32; ++i)
                         if (half * 64 + q * 32 + i >= valid) sr[q][i] = 0xff800000u;  // -inf
             }
-            // row max: combine the two halves of the row (slots alternate by block
-            // parity, so a fast thread never overwrites a value still to be read)
-            float* xm = xmax + (g & 1) * 2 * BLOCK_M;
+            // Exchange slots alternate with every exchange: a thread writes a slot
+            // again only after the next exchange, which its partner joins only after
+            // reading the slot.
+            // row max: combine the two halves of the row
+            float* xm = xslot();
             xm[half * BLOCK_M + row] = max64(sr);
             ok = pair_exchange();
             if (!ok) break;
@@ -443,9 +454,13 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
             } else {
                 m_use = m_run;
             }
-            // Lazy rescale of this thread's half of the O row (rare); PV(g-1)
-            // must have completed first.  Warp-uniform: TMEM access is collective.
-            if (__any_sync(0xffffffffu, rescale)) {
+            uint32_t pk[32];
+            const float sum = tail ? exp64<true>(sr, c, m_use, half * 64, valid, pk)
+                                   : exp64<false>(sr, c, m_use, half * 64, valid, pk);
+            const bool redo = __any_sync(0xffffffffu, rescale);  // warp-uniform
+            // Rescale of this thread's half of the O row (rare); PV(g-1) must have
+            // completed first.  Warp-uniform: TMEM access is collective.
+            if (redo) {
                 ok = warp_wait(bar(C::B_P_FREE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag, a.timeout_ns);
                 if (!ok) break;
                 tc_fence_after();
@@ -459,9 +474,6 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
                     tmem_st32(t_base + O_COL + half * DH + q * 32, orr);
                 }
             }
-            uint32_t pk[32];
-            const float sum = tail ? exp64<true>(sr, c, m_use, half * 64, valid, pk)
-                                   : exp64<false>(sr, c, m_use, half * 64, valid, pk);
             // P buffer sb is free once PV(g-2) has completed.
             if (g >= 2) {
                 ok = warp_wait(bar(C::B_P_FREE + sb), ((g >> 1) - 1) & 1, abort_flag, a.timeout_ns);
@@ -471,7 +483,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
             tmem_st32(t_base + P_COL + sb * 64u + half * 32, pk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_P_FULL + sb));
+            warp_arrive(bar(C::B_P_FULL + sb));
             l_run = l_run * alpha + sum;
             m_run = m_use;
         }
@@ -513,7 +525,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
             }
         }
         tc_fence_before();
-        mbar_arrive(bar(C::B_O_FREE));
+        warp_arrive(bar(C::B_O_FREE));
     }
 }
 
@@ -534,14 +546,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar0 + 8 * (C::B_Q_FULL + i), 1);   // (index 1 unused when Q_BUFS == 1)
             mbar_init(bar0 + 8 * (C::B_Q_FREE + i), 1);
             mbar_init(bar0 + 8 * (C::B_S_FULL + i), 1);
-            mbar_init(bar0 + 8 * (C::B_S_FREE + i), NUM_SOFTMAX);
-            mbar_init(bar0 + 8 * (C::B_P_FULL + i), NUM_SOFTMAX);
+            mbar_init(bar0 + 8 * (C::B_S_FREE + i), NUM_SOFTMAX_WARPS);
+            mbar_init(bar0 + 8 * (C::B_P_FULL + i), NUM_SOFTMAX_WARPS);
             mbar_init(bar0 + 8 * (C::B_P_FREE + i), 1);
         }
         mbar_init(bar0 + 8 * C::B_O_FINAL, 1);
-        mbar_init(bar0 + 8 * C::B_O_FREE, NUM_SOFTMAX);
+        mbar_init(bar0 + 8 * C::B_O_FREE, NUM_SOFTMAX_WARPS);
         mbar_init(bar0 + 8 * C::B_DRAIN, 2);
-        for (int q = 0; q < 4; ++q) mbar_init(bar0 + 8 * (C::B_PAIR + q), 64);
+        for (int q = 0; q < 4; ++q) mbar_init(bar0 + 8 * (C::B_PAIR + q), 2);
         for (int s = 0; s < C::KV_STAGES; ++s) {
             mbar_init(bar0 + 8 * (C::B_KV_FULL + s), 1);
             mbar_init(bar0 + 8 * (C::B_KV_FREE + s), 1);

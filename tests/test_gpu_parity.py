@@ -214,14 +214,20 @@ def _scaled_keys_case(xs, key_rows, factor, S=512, H=2, D=128, P=2, seed=11):
     assert_close(got, ref, mass, f"scaled keys {key_rows} x{factor}")
 
 
-def test_lazy_rescale_path(xs):
-    # first half of key block 1 scaled x4: its max exceeds the running max by > 8 (log2)
+def test_block_max_jump_first_half(xs):
+    # first half of key block 1 scaled x4: its max exceeds the running max by more
+    # than the lazy-rescale threshold, so O and l are rescaled
     _scaled_keys_case(xs, slice(128, 192), 4.0)
 
 
-def test_speculation_fallback_path(xs):
-    # second half of key block 1 scaled x16: exceeds the speculative max by > 32 (log2)
+def test_block_max_jump_second_half(xs):
+    # second half of key block 1 scaled x16: a very large jump, seen only by the
+    # threads that own the second half of the keys
     _scaled_keys_case(xs, slice(192, 256), 16.0)
+
+
+def test_block_max_jump_d64(xs):
+    _scaled_keys_case(xs, slice(128, 192), 24.0, S=640, H=4, D=64, P=4, seed=3)
 
 
 def test_growing_scores_every_block(xs):
