@@ -250,11 +250,18 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    fused = lambda: xs.xs_attn_a2a_fwd(q, k, v, outs, w.scale, stream)
-    alone = lambda: xs.xs_attn_fwd(q, k, v, contig, w.scale, stream)
+    # balanced schedule: the last partial wave of query tiles is spread over all
+    # SMs through a workspace (None when the tiles fill whole waves)
+    ws = xs.Workspace.for_shape(B, S, H, D, device=dev) if args.schedule == "balanced" else None
+
+    def fused():
+        xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_A2A, outs, w.scale, ws, stream)
+
+    def alone():
+        xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_CONTIGUOUS, [contig], w.scale, ws, stream)
 
     def serial_path():
-        xs.xs_attn_heads_fwd(q, k, v, heads, w.scale, stream)
+        xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_HEADS, heads, w.scale, ws, stream)
         xs.xs_relayout_a2a(heads, serial, stream)
 
     for _ in range(max(3, args.warmup)):
@@ -301,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
     pin = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).pin_memory()
     qh, kh, vh = pin(qb), pin(kb), pin(vb)
     out_h = [torch.empty(shard_shape, dtype=torch.bfloat16).pin_memory() for _ in range(P)]
-    e2e_fn = lambda: xs.xs_attn_a2a_fwd_staged(qh, kh, vh, out_h, q, k, v, outs, w.scale, stream)
+    e2e_fn = lambda: xs.xs_attn_a2a_fwd_staged(qh, kh, vh, out_h, q, k, v, outs, w.scale, workspace=ws, stream=stream)
     for _ in range(2):
         e2e_fn()
     n_e2e = max(3, min(args.steps, 20))
@@ -329,6 +336,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": B, "S": S, "H": H, "D": D, "P": P, "scale": w.scale,
                    "inputs": "seeded bf16 N(0,1)" + (" with outlier channels" if w.outliers else ""),
                    "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+                   "schedule": args.schedule, "workspace_bytes": ws.nbytes if ws else 0,
                    "parallelism": f"{world} independent replica(s), one GPU each" if world > 1 else "1 GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops if peak_tflops else None,
@@ -360,6 +368,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(di.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule", choices=["balanced", "plain"], default="balanced",
+                    help="balanced: spread the last partial wave of tiles over all SMs (workspace); "
+                         "plain: whole tiles only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
     args = ap.parse_args()

@@ -26,6 +26,9 @@ __all__ = [
     "xs_attn_heads_fwd",
     "xs_relayout_a2a",
     "xs_attn_a2a_fwd_staged",
+    "xs_attn_workspace_bytes",
+    "xs_attn_fwd_balanced",
+    "Workspace",
     "xs_attn_get_device_error",
     "xs_attn_error_string",
     "attn_a2a",
@@ -48,11 +51,17 @@ XS_ERR_SCALE = -8
 XS_ERR_CUDA = -9
 XS_ERR_DEVICE_TIMEOUT = -10
 XS_ERR_UNSUPPORTED_DEVICE = -11
+XS_ERR_WORKSPACE = -12
+XS_ERR_LAYOUT = -13
 XS_MAX_P = 16
+XS_LAYOUT_A2A = 0
+XS_LAYOUT_CONTIGUOUS = 1
+XS_LAYOUT_HEADS = 2
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
 _f32 = ctypes.c_float
+_size = ctypes.c_size_t
 
 # name -> (restype, argtypes); the full exported C ABI
 EXPORTS = {
@@ -61,7 +70,10 @@ EXPORTS = {
     "xs_attn_heads_fwd": (_int, [_vp, _vp, _vp, ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32, _vp]),
     "xs_relayout_a2a": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _vp]),
     "xs_attn_a2a_fwd_staged": (_int, [_vp, _vp, _vp, ctypes.POINTER(_vp), _vp, _vp, _vp, ctypes.POINTER(_vp),
-                                      _int, _int, _int, _int, _int, _f32, _vp]),
+                                      _int, _int, _int, _int, _int, _f32, _vp, _size, _vp]),
+    "xs_attn_workspace_bytes": (_int, [_int, _int, _int, _int, ctypes.POINTER(_size)]),
+    "xs_attn_fwd_balanced": (_int, [_vp, _vp, _vp, _int, ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32,
+                                    _vp, _size, _vp]),
     "xs_attn_get_device_error": (_int, [_vp]),
     "xs_attn_error_string": (ctypes.c_char_p, [_int]),
     "xs_attn_last_cuda_error": (_int, []),
@@ -157,14 +169,60 @@ def xs_relayout_a2a(heads, out_ptrs, stream=None) -> None:
 
 
 def xs_attn_a2a_fwd_staged(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, scale: float,
-                           stream=None) -> None:
-    """Host-resident variant: H2D copies, fused kernel and D2H copies of the shards, all on ``stream``."""
+                           workspace=None, stream=None) -> None:
+    """Host-resident variant: H2D copies, fused kernel and D2H copies of the shards, all on ``stream``.
+    ``workspace``: a :class:`Workspace` (balanced schedule) or None (plain schedule)."""
     B, S, H, D = q_host.shape
     P = len(out_dev)
+    wp, wn = _ws(workspace)
     _check(lib.xs_attn_a2a_fwd_staged(
         q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), _ptr_array([o.data_ptr() for o in out_host]),
         q_dev.data_ptr(), k_dev.data_ptr(), v_dev.data_ptr(), _ptr_array([o.data_ptr() for o in out_dev]),
-        B, S, H, D, P, scale, _stream_handle(stream)), "xs_attn_a2a_fwd_staged")
+        B, S, H, D, P, scale, wp, wn, _stream_handle(stream)), "xs_attn_a2a_fwd_staged")
+
+
+def xs_attn_workspace_bytes(B: int, S: int, H: int, D: int) -> int:
+    """Workspace bytes the balanced schedule needs for this shape on the current device (0: no split)."""
+    n = _size(0)
+    _check(lib.xs_attn_workspace_bytes(B, S, H, D, ctypes.byref(n)), "xs_attn_workspace_bytes")
+    return n.value
+
+
+class Workspace:
+    """A zero-filled device workspace for :func:`xs_attn_fwd_balanced` (torch-allocated,
+    256-byte aligned).  ``Workspace.for_shape(B, S, H, D)`` sizes it for one shape;
+    ``None`` is returned there when the shape needs none."""
+
+    def __init__(self, nbytes: int, device="cuda"):
+        import torch
+        self.nbytes = int(nbytes)
+        self._buf = torch.zeros(self.nbytes + 256, dtype=torch.uint8, device=device)
+        base = self._buf.data_ptr()
+        self.ptr = (base + 255) & ~255
+
+    @classmethod
+    def for_shape(cls, B: int, S: int, H: int, D: int, device="cuda"):
+        n = xs_attn_workspace_bytes(B, S, H, D)
+        return cls(n, device) if n else None
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return workspace.ptr, workspace.nbytes
+
+
+def xs_attn_fwd_balanced(q, k, v, layout: int, outs, scale: float, workspace, stream=None) -> None:
+    """The attention kernel with the last partial wave of tiles balanced over all SMs.
+    ``layout``: XS_LAYOUT_A2A (P sequence shards), XS_LAYOUT_CONTIGUOUS (one [B,S,H,D]
+    tensor) or XS_LAYOUT_HEADS (P head shards); ``workspace``: a :class:`Workspace` or None."""
+    B, S, H, D = _bshd(q, "q").shape
+    _bshd(k, "k"), _bshd(v, "v")
+    os_ = [_bshd(o, "out") for o in outs]
+    wp, wn = _ws(workspace)
+    _check(lib.xs_attn_fwd_balanced(q.data_ptr(), k.data_ptr(), v.data_ptr(), layout,
+                                    _ptr_array([o.data_ptr() for o in os_]), B, S, H, D, len(os_), scale, wp, wn,
+                                    _stream_handle(stream)), "xs_attn_fwd_balanced")
 
 
 def xs_attn_get_device_error(stream=None) -> int:
@@ -176,12 +234,16 @@ def xs_attn_error_string(code: int) -> str:
     return lib.xs_attn_error_string(code).decode()
 
 
-def attn_a2a(q, k, v, P: int, scale: float | None = None, stream=None):
-    """Allocate the P output shards with torch and run the fused path; returns the list of shards."""
+def attn_a2a(q, k, v, P: int, scale: float | None = None, stream=None, workspace=None):
+    """Allocate the P output shards with torch and run the fused path; returns the list of shards.
+    With a :class:`Workspace` the balanced schedule is used."""
     import torch
     B, S, H, D = q.shape
     if scale is None:
         scale = D ** -0.5
     outs = [torch.empty((B, S // P, H, D), dtype=torch.bfloat16, device=q.device) for _ in range(P)]
-    xs_attn_a2a_fwd(q, k, v, outs, scale, stream)
+    if workspace is None:
+        xs_attn_a2a_fwd(q, k, v, outs, scale, stream)
+    else:
+        xs_attn_fwd_balanced(q, k, v, XS_LAYOUT_A2A, outs, scale, workspace, stream)
     return outs

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -30,6 +32,7 @@ struct DeviceInfo {
     int sms = 0;
     int major = 0;
     int minor = 0;
+    int coop = 0;   // cooperative launches supported
 };
 
 constexpr int MAX_DEVICES = 64;
@@ -48,6 +51,8 @@ int device_info(DeviceInfo* out) {
         if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
             return cuda_fail(e);
         if ((e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
             return cuda_fail(e);
         d.known = true;
     }
@@ -168,11 +173,85 @@ unsigned long long timeout_ns() {
     return 1000000000ull;
 }
 
+// Work schedule of one attention launch.  Plain: grid = min(tiles, SMs), tile
+// u runs whole on CTA u % grid.  Balanced (needs a workspace): the whole waves
+// of tiles run as in the plain schedule, and the key-block iterations of the
+// tiles left over (tiles % SMs of them) are divided evenly over up to SMs CTAs,
+// at least MIN_PIECE blocks each; a tile cut among CTAs is merged in the kernel
+// through the workspace.  Used only when it shortens the last wave by at least
+// max(MIN_GAIN, n/8) key blocks per CTA.
+struct Plan {
+    int grid = 0;
+    bool split = false;
+    int dp_tiles = 0;
+    int sk_ctas = 0;
+    long long sk_iters = 0;
+    size_t off_ml = 0, off_flag = 0, ws_bytes = 0;   // workspace layout (split only)
+};
+
+constexpr long long MIN_PIECE = 8;    // key blocks per CTA range, at least
+constexpr long long MIN_GAIN = 16;    // key blocks a split must save per CTA, at least
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Plan make_plan(int B, int S, int H, int D, const DeviceInfo& dev) {
+    Plan pl;
+    const int n = (S + 127) / 128;
+    const int tiles = B * H * n;
+    const int G = dev.sms;
+    pl.grid = tiles < G ? tiles : G;
+    pl.dp_tiles = tiles;
+    const int rem = tiles % G;
+    if (!dev.coop || rem == 0) return pl;
+    const long long sk = static_cast<long long>(rem) * n;
+    long long ctas = sk / MIN_PIECE;
+    if (ctas > G) ctas = G;
+    if (ctas <= rem) return pl;   // no more CTAs busy than with whole tiles
+    // Each piece of work costs a fixed start (its Q tile, the pipeline fill) and a
+    // split tile its merge, a few key blocks' worth; measured on GB300 this eats
+    // the gain unless a range is shorter than a tile by max(16, n/8) blocks.
+    const long long range = (sk + ctas - 1) / ctas;
+    const long long gain_min = n / 8 > MIN_GAIN ? n / 8 : MIN_GAIN;
+    if (n - range < gain_min) return pl;
+    pl.split = true;
+    pl.dp_tiles = tiles - rem;
+    pl.sk_iters = sk;
+    pl.sk_ctas = static_cast<int>(ctas);
+    pl.grid = tiles >= G ? G : pl.sk_ctas;
+    // part_o [grid][128][D] fp32 | part_ml [grid][128] float2 | part_flag [grid][8] u32
+    const size_t slots = static_cast<size_t>(pl.grid);
+    pl.off_ml = align256(slots * 128 * D * 4);
+    pl.off_flag = pl.off_ml + align256(slots * 128 * 8);
+    pl.ws_bytes = pl.off_flag + align256(slots * 8 * 4);
+    return pl;
+}
+
+// Launch epochs mark the flags of split tiles.  They start at a per-process
+// value taken from the clock (so that flags left in a reused workspace by
+// another process are unlikely to match) and skip 0.
+std::atomic<unsigned> g_epoch{0};
+std::once_flag g_epoch_once;
+
+unsigned next_epoch() {
+    std::call_once(g_epoch_once, [] {
+        const auto t = std::chrono::high_resolution_clock::now().time_since_epoch().count();
+        g_epoch.store(static_cast<unsigned>(t ^ (t >> 32)) | 1u);
+    });
+    unsigned e = g_epoch.fetch_add(1) + 1;
+    if (e == 0) e = g_epoch.fetch_add(1) + 1;
+    return e;
+}
+
+// ws == nullptr: plain schedule.  Otherwise the balanced schedule whenever it
+// splits tiles; ws must then hold plan.ws_bytes bytes (256-byte aligned).
 int run_attention(const void* q, const void* k, const void* v, const xs::EpiParams& epi, int B, int S, int H, int D,
-                  float scale, cudaStream_t stream) {
+                  float scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
     DeviceInfo dev;
     int rc = device_info(&dev);
     if (rc != XS_OK) return rc;
+    const Plan pl = make_plan(B, S, H, D, dev);
+    const bool split = ws != nullptr && pl.split;
+    if (split && ws_bytes < pl.ws_bytes) return XS_ERR_WORKSPACE;
     CUtensorMap tq, tk, tv;
     if ((rc = encode_bshd(&tq, q, B, S, H, D)) != XS_OK) return rc;
     if ((rc = encode_bshd(&tk, k, B, S, H, D)) != XS_OK) return rc;
@@ -188,11 +267,88 @@ int run_attention(const void* q, const void* k, const void* v, const xs::EpiPara
     a.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.epi = epi;
     a.timeout_ns = timeout_ns();
-    const int grid = a.units < dev.sms ? a.units : dev.sms;
-    cudaError_t e = (D == 128) ? xs::launch_attn<128>(tq, tk, tv, a, grid, stream)
-                               : xs::launch_attn<64>(tq, tk, tv, a, grid, stream);
+    int grid = pl.grid;
+    if (split) {
+        char* base = static_cast<char*>(ws);
+        a.sp.dp_tiles = pl.dp_tiles;
+        a.sp.sk_iters = pl.sk_iters;
+        a.sp.sk_ctas = pl.sk_ctas;
+        a.sp.part_o = reinterpret_cast<float*>(base);
+        a.sp.part_ml = reinterpret_cast<float2*>(base + pl.off_ml);
+        a.sp.part_flag = reinterpret_cast<unsigned*>(base + pl.off_flag);
+        a.sp.epoch = next_epoch();
+    } else {
+        a.sp.dp_tiles = a.units;
+        grid = a.units < dev.sms ? a.units : dev.sms;
+    }
+    cudaError_t e = (D == 128) ? xs::launch_attn<128>(tq, tk, tv, a, grid, split, stream)
+                               : xs::launch_attn<64>(tq, tk, tv, a, grid, split, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return XS_OK;
+}
+
+// Output layout -> destination parameters and per-buffer byte size.
+int layout_epi(int layout, void* const* outs, int B, int S, int H, int D, int P, xs::EpiParams* epi, int* n_out,
+               int64_t* out_bytes, bool* need_div) {
+    std::memset(epi, 0, sizeof *epi);
+    const int np = (P >= 1 && P <= XS_MAX_P) ? P : 0;
+    switch (layout) {
+        case XS_LAYOUT_A2A:
+            *n_out = np;
+            *out_bytes = P >= 1 ? static_cast<int64_t>(B) * (S / P) * H * D * 2 : 0;
+            *need_div = true;
+            epi->Sl = P >= 1 ? S / P : S;
+            epi->Hl = H;
+            break;
+        case XS_LAYOUT_CONTIGUOUS:
+            *n_out = 1;
+            *out_bytes = static_cast<int64_t>(B) * S * H * D * 2;
+            *need_div = false;
+            epi->Sl = S;
+            epi->Hl = H;
+            break;
+        case XS_LAYOUT_HEADS:
+            *n_out = np;
+            *out_bytes = P >= 1 ? static_cast<int64_t>(B) * S * (H / P) * D * 2 : 0;
+            *need_div = true;
+            epi->Sl = S;
+            epi->Hl = P >= 1 ? H / P : H;
+            break;
+        default:
+            return XS_ERR_LAYOUT;
+    }
+    for (int i = 0; i < *n_out && outs; ++i) epi->ptr[i] = outs[i];
+    return XS_OK;
+}
+
+// Checks of a workspace given to a balanced call (after the shape checks).
+int check_workspace(const void* ws, size_t ws_bytes, const void* q, const void* k, const void* v, void* const* outs,
+                    int n_out, int64_t out_bytes, int B, int S, int H, int D) {
+    if (!ws) return XS_OK;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return XS_ERR_ALIGNMENT;
+    const int64_t in_bytes = static_cast<int64_t>(B) * S * H * D * 2;
+    const Range w = range_of(ws, static_cast<int64_t>(ws_bytes));
+    if (overlaps(w, range_of(q, in_bytes)) || overlaps(w, range_of(k, in_bytes)) || overlaps(w, range_of(v, in_bytes)))
+        return XS_ERR_OVERLAP;
+    for (int i = 0; i < n_out; ++i)
+        if (overlaps(w, range_of(outs[i], out_bytes))) return XS_ERR_OVERLAP;
+    return XS_OK;
+}
+
+int attn_layout_call(const void* q, const void* k, const void* v, int layout, void* const* outs, int B, int S, int H,
+                     int D, int P, float scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!outs) return XS_ERR_NULL;
+    xs::EpiParams epi;
+    int n_out = 0;
+    int64_t out_bytes = 0;
+    bool need_div = false;
+    int rc = layout_epi(layout, outs, B, S, H, D, P, &epi, &n_out, &out_bytes, &need_div);
+    if (rc != XS_OK) return rc;
+    rc = validate_attn(q, k, v, outs, n_out, B, S, H, D, layout == XS_LAYOUT_CONTIGUOUS ? 1 : P, scale, out_bytes,
+                       need_div);
+    if (rc != XS_OK) return rc;
+    if ((rc = check_workspace(ws, ws_bytes, q, k, v, outs, n_out, out_bytes, B, S, H, D)) != XS_OK) return rc;
+    return run_attention(q, k, v, epi, B, S, H, D, scale, ws, ws_bytes, stream);
 }
 
 }  // namespace
@@ -201,46 +357,37 @@ extern "C" {
 
 int xs_attn_a2a_fwd(const void* q, const void* k, const void* v, void* const* out_ptrs, int B, int S, int H, int D,
                     int P, float scale, void* stream) {
-    if (!out_ptrs) return XS_ERR_NULL;
-    const int n_out = (P >= 1 && P <= XS_MAX_P) ? P : 0;
-    const int64_t shard_bytes = (P >= 1) ? static_cast<int64_t>(B) * (S / P) * H * D * 2 : 0;
-    int rc = validate_attn(q, k, v, out_ptrs, n_out, B, S, H, D, P, scale, shard_bytes, true);
-    if (rc != XS_OK) return rc;
-    xs::EpiParams epi;
-    std::memset(&epi, 0, sizeof epi);
-    for (int p = 0; p < P; ++p) epi.ptr[p] = out_ptrs[p];
-    epi.Sl = S / P;
-    epi.Hl = H;
-    return run_attention(q, k, v, epi, B, S, H, D, scale, static_cast<cudaStream_t>(stream));
+    return attn_layout_call(q, k, v, XS_LAYOUT_A2A, out_ptrs, B, S, H, D, P, scale, nullptr, 0,
+                            static_cast<cudaStream_t>(stream));
 }
 
 int xs_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int S, int H, int D, float scale,
                 void* stream) {
     void* outs[1] = {out};
-    const int64_t bytes = static_cast<int64_t>(B) * S * H * D * 2;
-    int rc = validate_attn(q, k, v, outs, 1, B, S, H, D, 1, scale, bytes, false);
-    if (rc != XS_OK) return rc;
-    xs::EpiParams epi;
-    std::memset(&epi, 0, sizeof epi);
-    epi.ptr[0] = out;
-    epi.Sl = S;
-    epi.Hl = H;
-    return run_attention(q, k, v, epi, B, S, H, D, scale, static_cast<cudaStream_t>(stream));
+    return attn_layout_call(q, k, v, XS_LAYOUT_CONTIGUOUS, outs, B, S, H, D, 1, scale, nullptr, 0,
+                            static_cast<cudaStream_t>(stream));
 }
 
 int xs_attn_heads_fwd(const void* q, const void* k, const void* v, void* const* heads, int B, int S, int H, int D,
                       int P, float scale, void* stream) {
-    if (!heads) return XS_ERR_NULL;
-    const int n_out = (P >= 1 && P <= XS_MAX_P) ? P : 0;
-    const int64_t shard_bytes = (P >= 1) ? static_cast<int64_t>(B) * S * (H / P) * D * 2 : 0;
-    int rc = validate_attn(q, k, v, heads, n_out, B, S, H, D, P, scale, shard_bytes, true);
+    return attn_layout_call(q, k, v, XS_LAYOUT_HEADS, heads, B, S, H, D, P, scale, nullptr, 0,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int xs_attn_workspace_bytes(int B, int S, int H, int D, size_t* bytes) {
+    if (!bytes) return XS_ERR_NULL;
+    int rc = check_shape(B, S, H, D, 1, false);
     if (rc != XS_OK) return rc;
-    xs::EpiParams epi;
-    std::memset(&epi, 0, sizeof epi);
-    for (int p = 0; p < P; ++p) epi.ptr[p] = heads[p];
-    epi.Sl = S;
-    epi.Hl = H / P;
-    return run_attention(q, k, v, epi, B, S, H, D, scale, static_cast<cudaStream_t>(stream));
+    DeviceInfo dev;
+    if ((rc = device_info(&dev)) != XS_OK) return rc;
+    *bytes = make_plan(B, S, H, D, dev).ws_bytes;
+    return XS_OK;
+}
+
+int xs_attn_fwd_balanced(const void* q, const void* k, const void* v, int layout, void* const* outs, int B, int S,
+                         int H, int D, int P, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+    return attn_layout_call(q, k, v, layout, outs, B, S, H, D, P, scale, workspace, workspace_bytes,
+                            static_cast<cudaStream_t>(stream));
 }
 
 int xs_relayout_a2a(const void* const* heads, void* const* out_ptrs, int B, int S, int H, int D, int P,
@@ -280,7 +427,7 @@ int xs_relayout_a2a(const void* const* heads, void* const* out_ptrs, int B, int 
 
 int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v_host, void* const* out_host,
                            void* q_dev, void* k_dev, void* v_dev, void* const* out_dev, int B, int S, int H, int D,
-                           int P, float scale, void* stream) {
+                           int P, float scale, void* workspace, size_t workspace_bytes, void* stream) {
     if (!q_host || !k_host || !v_host || !out_host || !out_dev) return XS_ERR_NULL;
     if (P >= 1 && P <= XS_MAX_P)
         for (int p = 0; p < P; ++p)
@@ -289,13 +436,18 @@ int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v
     const int64_t shard_bytes = (P >= 1) ? static_cast<int64_t>(B) * (S / P) * H * D * 2 : 0;
     int rc = validate_attn(q_dev, k_dev, v_dev, out_dev, n_out, B, S, H, D, P, scale, shard_bytes, true);
     if (rc != XS_OK) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, q_dev, k_dev, v_dev, out_dev, n_out, shard_bytes, B, S, H,
+                              D)) != XS_OK)
+        return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t in_bytes = static_cast<size_t>(B) * S * H * D * 2;
     cudaError_t e;
     if ((e = cudaMemcpyAsync(q_dev, q_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMemcpyAsync(k_dev, k_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMemcpyAsync(v_dev, v_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
-    if ((rc = xs_attn_a2a_fwd(q_dev, k_dev, v_dev, out_dev, B, S, H, D, P, scale, stream)) != XS_OK) return rc;
+    if ((rc = xs_attn_fwd_balanced(q_dev, k_dev, v_dev, XS_LAYOUT_A2A, out_dev, B, S, H, D, P, scale, workspace,
+                                   workspace_bytes, stream)) != XS_OK)
+        return rc;
     for (int p = 0; p < P; ++p)
         if ((e = cudaMemcpyAsync(out_host[p], out_dev[p], static_cast<size_t>(shard_bytes), cudaMemcpyDeviceToHost,
                                  st)) != cudaSuccess)
@@ -325,6 +477,8 @@ const char* xs_attn_error_string(int code) {
         case XS_ERR_CUDA: return "a CUDA call or kernel launch failed (see xs_attn_last_cuda_error)";
         case XS_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel expired; the launch was abandoned";
         case XS_ERR_UNSUPPORTED_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
+        case XS_ERR_WORKSPACE: return "the workspace is smaller than xs_attn_workspace_bytes reports";
+        case XS_ERR_LAYOUT: return "unknown output layout";
         default: return "unknown xsattn error code";
     }
 }

@@ -168,6 +168,59 @@ __device__ __forceinline__ void decode_unit(int u, const AttnArgs& a, int& b, in
     b = bh / a.H;
 }
 
+// One piece of work of a CTA: key blocks [k0, k0 + nb) of query tile (b, h, qt).
+enum WorkKind { WORK_FULL = 0, WORK_HEAD = 1, WORK_PART = 2 };
+struct Work {
+    int b, h, qt;
+    int k0, nb;
+    int kind;   // WORK_FULL: the whole tile; WORK_HEAD: blocks [0, k) of a split
+                // tile, merged with the parts of the following CTAs and stored;
+                // WORK_PART: blocks [k0, k0 + nb), k0 > 0, of a split tile,
+                // published as a partial result
+    int t_sk;   // index of the tile among the split-scheduled tiles (-1: whole wave)
+};
+
+// Start of CTA i's range of split-scheduled key-block iterations.
+__device__ __forceinline__ long long sk_start(const AttnArgs& a, int i) {
+    return a.sp.sk_iters * i / a.sp.sk_ctas;
+}
+
+// The idx-th piece of work of this CTA (every role walks the same sequence):
+// first its whole tiles cta, cta + grid, ... below dp_tiles, then the pieces of
+// its range [sk_start(cta), sk_start(cta + 1)) of the remaining tiles'
+// key-block iterations (CTAs from sk_ctas on have none).  A range holds at most
+// one part (its first piece, when it starts inside a tile) and at most one head
+// (its last piece, when it ends inside a tile that it entered at block 0).
+__device__ __forceinline__ bool get_work(const AttnArgs& a, int idx, Work& w) {
+    const int G = static_cast<int>(gridDim.x);
+    const int i = static_cast<int>(blockIdx.x);
+    const int n = a.n_kv;
+    const int dp = a.sp.dp_tiles;
+    const int ndp = dp > i ? (dp - i + G - 1) / G : 0;
+    int tile, k0 = 0, k1 = n;
+    if (idx < ndp) {
+        tile = i + idx * G;
+        w.kind = WORK_FULL;
+        w.t_sk = -1;
+    } else {
+        if (a.sp.sk_iters == 0 || i >= a.sp.sk_ctas) return false;
+        const long long it0 = sk_start(a, i), it1 = sk_start(a, i + 1);
+        if (it1 <= it0) return false;
+        const long long t = it0 / n + (idx - ndp);
+        if (t > (it1 - 1) / n) return false;
+        const long long lo = it0 - t * n, hi = it1 - t * n;
+        k0 = lo > 0 ? static_cast<int>(lo) : 0;
+        k1 = hi < n ? static_cast<int>(hi) : n;
+        tile = dp + static_cast<int>(t);
+        w.kind = k0 > 0 ? WORK_PART : (k1 == n ? WORK_FULL : WORK_HEAD);
+        w.t_sk = static_cast<int>(t);
+    }
+    decode_unit(tile, a, w.b, w.h, w.qt);
+    w.k0 = k0;
+    w.nb = k1 - k0;
+    return true;
+}
+
 // Ring item `i` of a unit with n key blocks, in the consumption order
 // K0, K1, V0, K2, V1, K3, ..., V(n-3), K(n-1), V(n-2), V(n-1): the block index
 // and whether it is a V block.
@@ -205,10 +258,9 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     int u_iter = 0;
     int q_last = -1;          // u_iter of the last Q load issued
     bool ok = true;
-    const int n = a.n_kv;
-    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++u_iter) {
-        int b, h, qt;
-        decode_unit(u, a, b, h, qt);
+    Work w;
+    for (; ok && get_work(a, u_iter, w); ++u_iter) {
+        const int b = w.b, h = w.h, qt = w.qt;
         const int qb = u_iter % C::Q_BUFS;
         if (u_iter >= C::Q_BUFS)
             ok = thread_wait(bar(C::B_Q_FREE + qb), ((u_iter / C::Q_BUFS) - 1) & 1, abort_flag, a.timeout_ns);
@@ -218,10 +270,17 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
             tma_load_4d(sbase + C::Q_OFF + qb * C::TILE_BYTES + pnl * PANEL_BYTES, tq, bar(C::B_Q_FULL + qb),
                         pnl * 64, h, qt * BLOCK_M, b);
         q_last = u_iter;
-        for (int i = 0; i < 2 * n && ok; ++i) {
+        {   // start the next piece's Q towards L2: its load waits for this piece's
+            // last S MMA (one Q buffer at D = 128) and then hits L2, not HBM
+            Work wn;
+            if (get_work(a, u_iter + 1, wn))
+                for (int pnl = 0; pnl < C::PANELS; ++pnl) tma_prefetch_l2_4d(tq, pnl * 64, wn.h, wn.qt * BLOCK_M, wn.b);
+        }
+        for (int i = 0; i < 2 * w.nb && ok; ++i) {
             int blk;
             bool is_v;
-            ring_item(i, n, blk, is_v);
+            ring_item(i, w.nb, blk, is_v);
+            blk += w.k0;
             const uint32_t stage = item % C::KV_STAGES;
             const uint32_t round = item / C::KV_STAGES;
             if (round > 0) ok = thread_wait(bar(C::B_KV_FREE + stage), (round - 1) & 1, abort_flag, a.timeout_ns);
@@ -265,14 +324,15 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
     constexpr uint32_t IDESC_QK = idesc_bf16_f32(BLOCK_M, BLOCK_N, 0);
-    const int n = a.n_kv;
     uint32_t g = 0;      // key blocks over the CTA's lifetime
+    uint32_t item0 = 0;  // first ring item of the current piece of work
     int u_iter = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++u_iter) {
+    Work w;
+    for (; ok && get_work(a, u_iter, w); ++u_iter) {
+        const int n = w.nb;
         const int qb = u_iter % C::Q_BUFS;
         const uint32_t qaddr = sbase + C::Q_OFF + qb * C::TILE_BYTES;
-        const uint32_t item0 = static_cast<uint32_t>(u_iter) * 2u * n;
         ok = thread_wait(bar(C::B_Q_FULL + qb), (u_iter / C::Q_BUFS) & 1, abort_flag, a.timeout_ns);
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gs = g + j;
@@ -293,11 +353,13 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
             if (j == n - 1) mma_commit(bar(C::B_Q_FREE + qb));
         }
         g += n;
+        item0 += 2u * n;
     }
-    // Drain: B_DRAIN completes when both issuers' MMAs have all completed.
+    // Drain: B_DRAIN completes when both issuers' MMAs have all completed (TMEM
+    // is freed after it).  The limit is at least 20 ms whatever the wait limit.
     mma_commit(bar(C::B_DRAIN));
     volatile int no_abort = 0;
-    thread_wait(bar(C::B_DRAIN), 0, &no_abort, ok ? a.timeout_ns : 20000000ull);
+    thread_wait(bar(C::B_DRAIN), 0, &no_abort, a.timeout_ns > 20000000ull ? a.timeout_ns : 20000000ull);
 }
 
 // Issuer of PV(j): O += P(j) V_j (A = P buffer from TMEM).  One thread.
@@ -308,12 +370,13 @@ __device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uin
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
     constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 1);
-    const int n = a.n_kv;
     uint32_t g = 0;
+    uint32_t item0 = 0;
     int u_iter = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++u_iter) {
-        const uint32_t item0 = static_cast<uint32_t>(u_iter) * 2u * n;
+    Work w;
+    for (; ok && get_work(a, u_iter, w); ++u_iter) {
+        const int n = w.nb;
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gj = g + j;
             const uint32_t pb = gj & 1;
@@ -335,13 +398,36 @@ __device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uin
             if (j == n - 1) mma_commit(bar(C::B_O_FINAL));
         }
         g += n;
+        item0 += 2u * n;
     }
     mma_commit(bar(C::B_DRAIN));
     volatile int no_abort = 0;
-    thread_wait(bar(C::B_DRAIN), 0, &no_abort, ok ? a.timeout_ns : 20000000ull);
+    thread_wait(bar(C::B_DRAIN), 0, &no_abort, a.timeout_ns > 20000000ull ? a.timeout_ns : 20000000ull);
 }
 
 // ------------------------------------------------------- softmax + epilogue
+// Bounded wait (whole warp) until every softmax warp of CTA `slot` has published
+// its part of a split tile in this launch.  Each lane polls the eight flags
+// itself with acquire loads, so its later loads of the partial are ordered
+// after them.  The result is warp-uniform.
+__device__ __forceinline__ bool wait_partial(const AttnArgs& a, int slot, volatile int* abort_flag) {
+    const unsigned* f = a.sp.part_flag + slot * NUM_SOFTMAX_WARPS;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        bool mine = true;
+#pragma unroll
+        for (int i = 0; i < NUM_SOFTMAX_WARPS; ++i) mine = mine && (ld_acquire_gpu(f + i) == a.sp.epoch);
+        if (__all_sync(0xffffffffu, mine)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 >= a.timeout_ns) {
+            *abort_flag = 1;
+            atomicCAS(&g_device_error, 0, XS_DEVICE_TIMEOUT_CODE);
+            return false;
+        }
+        __nanosleep(256);
+    }
+}
+
 // Maximum of a thread's 64 scores: four independent 3-input chains.
 __device__ __forceinline__ float max64(const uint32_t (&sr)[2][32]) {
     float mx[4];
@@ -383,6 +469,97 @@ __device__ __forceinline__ float exp64(const uint32_t (&sr)[2][32], float c, flo
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
+// Epilogue of a piece of a split tile (rare: at most two per CTA and launch),
+// kept out of line so that it does not weigh on the register allocation of the
+// softmax loop.  The calling thread owns query row `row` of the tile and the DH
+// output columns at TMEM address o_cols (half `half` of the row); m, l are the
+// row's running max (log2 units) and sum over this piece's key blocks.
+//   WORK_PART: publish the unnormalised O, m and l in this CTA's workspace slot,
+//              then this warp's flag (release) with the launch epoch.
+//   WORK_HEAD: wait for the parts of the tile (slots of the following CTAs whose
+//              ranges start inside it) and store
+//              (sum_k O_k 2^(m_k - M)) / (sum_k l_k 2^(m_k - M)),  M = max_k m_k,
+//              over this piece and the parts.
+template <int D>
+__device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, uint32_t o_cols, int row, int half,
+                                            int warp, float m, float l, volatile int* abort_flag) {
+    constexpr int DH = D / 2;
+    if (w.kind == WORK_PART) {
+        float* po = a.sp.part_o + (static_cast<size_t>(blockIdx.x) * BLOCK_M + row) * D + half * DH;
+#pragma unroll 1
+        for (int q = 0; q < DH / 32; ++q) {
+            uint32_t orr[32];
+            tmem_ld32(o_cols + q * 32, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+                st_global_v4(po + q * 32 + v4 * 4, orr[4 * v4], orr[4 * v4 + 1], orr[4 * v4 + 2], orr[4 * v4 + 3]);
+        }
+        if (half == 0) a.sp.part_ml[static_cast<size_t>(blockIdx.x) * BLOCK_M + row] = make_float2(m, l);
+        __syncwarp();
+        if (lane_id() == 0) {
+            __threadfence();
+            st_release_gpu(a.sp.part_flag + blockIdx.x * NUM_SOFTMAX_WARPS + warp, a.sp.epoch);
+        }
+        return true;
+    }
+    // the parts: CTAs j = blockIdx.x + 1, ... whose ranges start before the tile's end
+    const long long tile_end = static_cast<long long>(w.t_sk + 1) * a.n_kv;
+    const int j0 = blockIdx.x + 1;
+    int j1 = j0;
+    while (j1 < a.sp.sk_ctas && sk_start(a, j1) < tile_end) ++j1;
+    float m_all = m;
+    for (int j = j0; j < j1; ++j) {
+        if (!wait_partial(a, j, abort_flag)) return false;
+        m_all = fmaxf(m_all, a.sp.part_ml[static_cast<size_t>(j) * BLOCK_M + row].x);
+    }
+    const float f_own = ex2_approx(m - m_all);
+    float l_all = l * f_own;
+    for (int j = j0; j < j1; ++j) {
+        const float2 ml = a.sp.part_ml[static_cast<size_t>(j) * BLOCK_M + row];
+        l_all += ml.y * ex2_approx(ml.x - m_all);
+    }
+    const float inv_l = 1.0f / l_all;
+    const int s_row = w.qt * BLOCK_M + row;
+    const bool store = s_row < a.S;
+    __nv_bfloat16* dst = nullptr;
+    if (store) {
+        const int p = s_row / a.epi.Sl + w.h / a.epi.Hl;
+        dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
+              ((static_cast<size_t>(w.b) * a.epi.Sl + s_row % a.epi.Sl) * a.epi.Hl + w.h % a.epi.Hl) * D + half * DH;
+    }
+#pragma unroll 1
+    for (int q = 0; q < DH / 32; ++q) {
+        uint32_t orr[32];
+        tmem_ld32(o_cols + q * 32, orr);
+        tmem_wait_ld();
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(orr[i]) * f_own;
+        for (int j = j0; j < j1; ++j) {
+            const float f = ex2_approx(a.sp.part_ml[static_cast<size_t>(j) * BLOCK_M + row].x - m_all);
+            const float* po = a.sp.part_o + (static_cast<size_t>(j) * BLOCK_M + row) * D + half * DH + q * 32;
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+                const float4 pv = *reinterpret_cast<const float4*>(po + v4 * 4);
+                acc[4 * v4 + 0] += pv.x * f;
+                acc[4 * v4 + 1] += pv.y * f;
+                acc[4 * v4 + 2] += pv.z * f;
+                acc[4 * v4 + 3] += pv.w * f;
+            }
+        }
+        uint32_t wv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wv[i] = pack_bf16x2(acc[2 * i] * inv_l, acc[2 * i + 1] * inv_l);
+        if (store) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+                st_global_v4(dst + q * 32 + v4 * 8, wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
+        }
+    }
+    return true;
+}
+
 template <int D>
 __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
                              volatile int* abort_flag) {
@@ -397,7 +574,6 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
     float* xsum = reinterpret_cast<float*>(smem + C::XCH_OFF + C::XMAX_BYTES);  // [2][128]
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
     const float c = a.c;
-    const int n = a.n_kv;
     // Exchange with the other thread of this row (the warp 4 apart): both
     // threads have stored their value to shared memory before either reads.
     uint32_t xchg = 0;
@@ -410,9 +586,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
     uint32_t g = 0;
     int u_iter = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++u_iter) {
-        int b, h, qt;
-        decode_unit(u, a, b, h, qt);
+    while (ok) {
+        int n, valid0;   // only these two stay live through the block loop
+        {
+            Work w;
+            if (!get_work(a, u_iter, w)) break;
+            n = w.nb;
+            valid0 = a.S - w.k0 * BLOCK_N;
+        }
         float m_run = 0.0f, l_run = 0.0f;
         for (int j = 0; j < n; ++j, ++g) {
             const uint32_t sb = g & 1;
@@ -425,7 +606,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
             tmem_wait_ld();
             tc_fence_before();
             warp_arrive(bar(C::B_S_FREE + sb));  // the MMA may now overwrite this S buffer
-            const int valid = a.S - j * BLOCK_N;
+            const int valid = valid0 - j * BLOCK_N;
             const bool tail = valid < BLOCK_N;
             if (tail) {
 #pragma unroll
@@ -495,37 +676,46 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
         ok = pair_exchange();
         if (!ok) break;
         const float l_row = xsum[row] + xsum[BLOCK_M + row];
+        Work w;
+        get_work(a, u_iter, w);   // the same piece of work as above (recomputed, not kept live)
+        const int b = w.b, h = w.h, qt = w.qt;
         ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns);
         if (!ok) break;
         tc_fence_after();
-        const int s_row = qt * BLOCK_M + row;
-        const bool store = s_row < a.S;
-        __nv_bfloat16* dst = nullptr;
-        if (store) {
-            const int p = s_row / a.epi.Sl + h / a.epi.Hl;
-            const int s_dst = s_row % a.epi.Sl;
-            const int h_dst = h % a.epi.Hl;
-            dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
-                  ((static_cast<size_t>(b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D + half * DH;
-        }
-        const float inv_l = 1.0f / l_row;
-#pragma unroll
-        for (int q = 0; q < DH / 32; ++q) {
-            uint32_t orr[32];
-            tmem_ld32(t_base + O_COL + half * DH + q * 32, orr);
-            tmem_wait_ld();
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                w[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
+        if (w.kind == WORK_FULL) {
+            const int s_row = qt * BLOCK_M + row;
+            const bool store = s_row < a.S;
+            __nv_bfloat16* dst = nullptr;
             if (store) {
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                    st_global_v4(dst + q * 32 + v4 * 8, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                const int p = s_row / a.epi.Sl + h / a.epi.Hl;
+                const int s_dst = s_row % a.epi.Sl;
+                const int h_dst = h % a.epi.Hl;
+                dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
+                      ((static_cast<size_t>(b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D + half * DH;
             }
+            const float inv_l = 1.0f / l_row;
+#pragma unroll
+            for (int q = 0; q < DH / 32; ++q) {
+                uint32_t orr[32];
+                tmem_ld32(t_base + O_COL + half * DH + q * 32, orr);
+                tmem_wait_ld();
+                uint32_t wv[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    wv[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
+                if (store) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        st_global_v4(dst + q * 32 + v4 * 8, wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
+                }
+            }
+        } else {
+            ok = split_epilogue<D>(a, w, t_base + O_COL + half * DH, row, half, warp, m_run, l_row, abort_flag);
+            if (!ok) break;
         }
         tc_fence_before();
         warp_arrive(bar(C::B_O_FREE));
+        ++u_iter;
     }
 }
 
@@ -606,20 +796,29 @@ static_assert(Cfg<64>::SMEM_ALLOC <= 232448, "shared memory budget (D = 64)");
 
 template <int D>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& args,
-                        int grid, cudaStream_t stream) {
+                        int grid, bool cooperative, cudaStream_t stream) {
     auto kern = attn_a2a_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, args);
-    return cudaGetLastError();
+    if (!cooperative) {
+        kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, args);
+        return cudaGetLastError();
+    }
+    // CTAs of a split tile wait for each other: all of them must be resident at
+    // once, which a cooperative launch guarantees (or refuses to launch).
+    CUtensorMap q = tq, k = tk, v = tv;
+    AttnArgs a = args;
+    void* params[] = {&q, &k, &v, &a};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(NUM_THREADS), params,
+                                       Cfg<D>::SMEM_ALLOC, stream);
 }
 
 template int attn_smem_bytes<64>();
 template int attn_smem_bytes<128>();
 template cudaError_t launch_attn<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const AttnArgs&, int,
-                                     cudaStream_t);
+                                     bool, cudaStream_t);
 template cudaError_t launch_attn<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const AttnArgs&,
-                                      int, cudaStream_t);
+                                      int, bool, cudaStream_t);
 
 cudaError_t read_and_clear_device_error(int* value) {
     int zero = 0;

@@ -23,22 +23,45 @@ struct EpiParams {
     int Hl;
 };
 
+// Balanced ("stream-K") schedule of the tiles left over after the whole waves.
+// Tiles [0, dp_tiles) run whole, tile = cta + w * grid.  The key-block
+// iterations of tiles [dp_tiles, units) (sk_iters = their count * n_kv,
+// tile-major) are cut into sk_ctas contiguous ranges, range i for CTA i; a range
+// may start or end inside a tile, and a tile may be cut among several CTAs.
+// Every piece that starts inside a tile (a "part") writes its unnormalised
+// partial result to slot `its CTA index` of the workspace and publishes it with
+// `epoch` in one flag per softmax warp; the piece that starts the tile (the
+// "head", done last by its CTA) waits for the parts of the CTAs after it whose
+// ranges start inside the tile and merges them.  sk_iters == 0: no split.
+struct SplitParams {
+    int dp_tiles;
+    int sk_ctas;
+    long long sk_iters;
+    float* part_o;         // [grid][128][D] fp32 partial numerators
+    float2* part_ml;       // [grid][128] (running max in log2 units, row sum)
+    unsigned* part_flag;   // [grid][8] epoch of the publishing softmax warp
+    unsigned epoch;        // this launch's epoch (never 0)
+};
+
 struct AttnArgs {
     int B, S, H;
     int n_kv;       // ceil(S / 128) key blocks
-    int n_qt;       // ceil(S / 128) query tiles (work units) per (b, h)
-    int units;      // B * H * n_qt
+    int n_qt;       // ceil(S / 128) query tiles per (b, h)
+    int units;      // B * H * n_qt tiles
     float c;        // scale * log2(e)
     EpiParams epi;
     unsigned long long timeout_ns;  // limit for every wait inside the kernel
+    SplitParams sp;
 };
 
 template <int D>
 int attn_smem_bytes();
 
+// cooperative: launch with the co-residency guarantee (needed whenever
+// args.sp.sk_iters != 0, because CTAs then wait for each other).
 template <int D>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const AttnArgs& args, int grid, cudaStream_t stream);
+                        const AttnArgs& args, int grid, bool cooperative, cudaStream_t stream);
 
 cudaError_t read_and_clear_device_error(int* value);
 

@@ -60,7 +60,17 @@ enum {
     XS_ERR_SCALE = -8,           /* scale is NaN or infinite                            */
     XS_ERR_CUDA = -9,            /* a CUDA runtime/driver call or launch failed         */
     XS_ERR_DEVICE_TIMEOUT = -10, /* a bounded wait inside a kernel ran out; see below   */
-    XS_ERR_UNSUPPORTED_DEVICE = -11 /* the current device is not sm_103 (GB300)        */
+    XS_ERR_UNSUPPORTED_DEVICE = -11, /* the current device is not sm_103 (GB300)       */
+    XS_ERR_WORKSPACE = -12,      /* the workspace is smaller than required              */
+    XS_ERR_LAYOUT = -13          /* unknown output layout                               */
+};
+
+/* Output layouts of xs_attn_fwd_balanced (the three layouts of the entry points
+ * below: sequence shards, one contiguous tensor, Ulysses head shards). */
+enum {
+    XS_LAYOUT_A2A = 0,         /* outs[p]: [B, S/P, H, D], as xs_attn_a2a_fwd      */
+    XS_LAYOUT_CONTIGUOUS = 1,  /* outs[0]: [B, S, H, D], as xs_attn_fwd (P ignored) */
+    XS_LAYOUT_HEADS = 2        /* outs[r]: [B, S, H/P, D], as xs_attn_heads_fwd    */
 };
 
 /*
@@ -122,12 +132,61 @@ int xs_relayout_a2a(const void* const* heads, void* const* out_ptrs,
  * caller's device shards out_dev[p], and copies every shard back into the host
  * buffers out_host[p]; all on `stream`, in that order.  The host buffers must
  * stay alive and untouched until the stream has finished.  Device-side rules
- * are those of xs_attn_a2a_fwd.
+ * are those of xs_attn_a2a_fwd; workspace / workspace_bytes are those of
+ * xs_attn_fwd_balanced (NULL, 0: the plain schedule).
  */
 int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v_host,
                            void* const* out_host,
                            void* q_dev, void* k_dev, void* v_dev, void* const* out_dev,
-                           int B, int S, int H, int D, int P, float scale, void* stream);
+                           int B, int S, int H, int D, int P, float scale,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * xs_attn_workspace_bytes -- device workspace that xs_attn_fwd_balanced needs
+ * for this shape on the current device (0 when the tiles already fill whole
+ * waves and nothing is split).  The value depends only on the device's SM
+ * count, D and whether the shape splits: with G SMs it is about
+ * G * (512*D + 1056) bytes (10.1 MB at D = 128 on 152 SMs).
+ *   bytes  host pointer that receives the size.
+ * Returns XS_OK, XS_ERR_NULL, a shape error, XS_ERR_UNSUPPORTED_DEVICE or
+ * XS_ERR_CUDA.
+ */
+int xs_attn_workspace_bytes(int B, int S, int H, int D, size_t* bytes);
+
+/*
+ * xs_attn_fwd_balanced -- the attention kernel of the three entry points above
+ * (layout XS_LAYOUT_A2A, _CONTIGUOUS or _HEADS, same outputs and rules) with
+ * the last, partial wave of query tiles balanced over all SMs.
+ * The kernel is persistent, one CTA per SM, and a 128-row query tile is its unit
+ * of work; when the tile count is not a multiple of the SM count, the plain
+ * schedule leaves SMs idle in the last wave.  Here the first
+ * floor(tiles/SMs) - 1 waves run whole tiles and the key blocks of the
+ * remaining tiles are divided evenly over all SMs ("stream-K"); a tile whose
+ * key range is cut between two CTAs is completed by both: the later CTA writes
+ * its unnormalised partial output (fp32), running max and row sum to the
+ * workspace and publishes them with a per-launch epoch, the earlier CTA waits
+ * for them (a bounded wait) and merges:
+ *     O = (O_1 2^(m_1-m) + O_2 2^(m_2-m)) / (l_1 2^(m_1-m) + l_2 2^(m_2-m)),
+ *     m = max(m_1, m_2).
+ * The merge reorders fp32 sums, so results agree with the plain schedule to
+ * rounding, not bit for bit; the three layouts stay bit-identical to each other.
+ *   workspace        device buffer, 256-byte aligned, of at least
+ *                    xs_attn_workspace_bytes(B, S, H, D) bytes, not overlapping
+ *                    any input or output; NULL selects the plain schedule.
+ *                    Contents: scratch owned by the library during the call.
+ *                    It must be zero-filled once before its first use (the
+ *                    flags of a launch are recognised by their epoch, and a
+ *                    zero flag never matches one).  Two calls may share a
+ *                    workspace only if they are ordered (same stream, or
+ *                    synchronised); concurrent calls on one workspace race.
+ *   workspace_bytes  its size in bytes; smaller than required ->
+ *                    XS_ERR_WORKSPACE (nothing launched).
+ * When a tile is split the kernel is launched cooperatively (all CTAs resident
+ * at once); CTAs then wait for each other only through bounded waits.
+ */
+int xs_attn_fwd_balanced(const void* q, const void* k, const void* v, int layout, void* const* outs,
+                         int B, int S, int H, int D, int P, float scale,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * xs_attn_get_device_error -- synchronises `stream`, then reads and clears the

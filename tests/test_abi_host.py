@@ -122,10 +122,46 @@ def test_heads_and_relayout_validation(xs):
 def test_staged_validation(xs):
     lib = xs.lib
     host = _outs(2, base=0x70_0000_0000)
-    assert lib.xs_attn_a2a_fwd_staged(None, 1, 1, host, Q, K, V, _outs(2), 1, 256, 2, 64, 2, 0.1, None) == xs.XS_ERR_NULL
+    assert lib.xs_attn_a2a_fwd_staged(None, 1, 1, host, Q, K, V, _outs(2), 1, 256, 2, 64, 2, 0.1,
+                                      None, 0, None) == xs.XS_ERR_NULL
     host3 = _outs(3, base=0x70_0000_0000)
-    assert lib.xs_attn_a2a_fwd_staged(16, 16, 16, host3, Q, K, V, _outs(3), 1, 256, 2, 64, 3, 0.1, None) == \
+    assert lib.xs_attn_a2a_fwd_staged(16, 16, 16, host3, Q, K, V, _outs(3), 1, 256, 2, 64, 3, 0.1,
+                                      None, 0, None) == xs.XS_ERR_DIVISIBILITY
+    # a workspace that overlaps an input is refused before anything runs
+    assert lib.xs_attn_a2a_fwd_staged(16, 16, 16, host, Q, K, V, _outs(2), 1, 256, 2, 64, 2, 0.1,
+                                      Q, 1 << 20, None) == xs.XS_ERR_OVERLAP
+
+
+def test_balanced_validation(xs):
+    lib = xs.lib
+    WS = 0x60_0000_0000
+    outs = _outs(2)
+    # unknown layout
+    assert lib.xs_attn_fwd_balanced(Q, K, V, 7, outs, 1, 256, 2, 64, 2, 0.1, WS, 1 << 20, None) == xs.XS_ERR_LAYOUT
+    # layouts keep the checks of their plain entry points
+    assert lib.xs_attn_fwd_balanced(Q, K, V, xs.XS_LAYOUT_A2A, outs, 1, 256, 3, 64, 2, 0.1, WS, 1 << 20, None) == \
         xs.XS_ERR_DIVISIBILITY
+    assert lib.xs_attn_fwd_balanced(Q, K, V, xs.XS_LAYOUT_HEADS, outs, 1, 255, 2, 64, 2, 0.1, WS, 1 << 20, None) == \
+        xs.XS_ERR_DIVISIBILITY
+    assert lib.xs_attn_fwd_balanced(Q, K, V, xs.XS_LAYOUT_A2A, None, 1, 256, 2, 64, 2, 0.1, WS, 1 << 20, None) == \
+        xs.XS_ERR_NULL
+    # the workspace must be 256-byte aligned and disjoint from inputs and outputs
+    assert lib.xs_attn_fwd_balanced(Q, K, V, xs.XS_LAYOUT_A2A, outs, 1, 256, 2, 64, 2, 0.1, WS + 16, 1 << 20,
+                                    None) == xs.XS_ERR_ALIGNMENT
+    assert lib.xs_attn_fwd_balanced(Q, K, V, xs.XS_LAYOUT_A2A, outs, 1, 256, 2, 64, 2, 0.1, K - 4096, 1 << 20,
+                                    None) == xs.XS_ERR_OVERLAP
+    ptrs = [outs[i] for i in range(2)]
+    assert lib.xs_attn_fwd_balanced(Q, K, V, xs.XS_LAYOUT_A2A, outs, 1, 256, 2, 64, 2, 0.1, ptrs[1], 1 << 20,
+                                    None) == xs.XS_ERR_OVERLAP
+
+
+def test_workspace_query_validation(xs):
+    import ctypes
+    lib = xs.lib
+    n = ctypes.c_size_t(0)
+    assert lib.xs_attn_workspace_bytes(1, 256, 2, 64, None) == xs.XS_ERR_NULL
+    assert lib.xs_attn_workspace_bytes(1, 256, 2, 48, ctypes.byref(n)) == xs.XS_ERR_HEAD_DIM
+    assert lib.xs_attn_workspace_bytes(0, 256, 2, 64, ctypes.byref(n)) == xs.XS_ERR_SHAPE
 
 
 def test_python_binding_rejects_cpu_tensors(xs):
