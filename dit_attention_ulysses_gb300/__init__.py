@@ -28,6 +28,7 @@ __all__ = [
     "xs_attn_a2a_fwd_staged",
     "xs_attn_workspace_bytes",
     "xs_attn_fwd_balanced",
+    "xs_attn_fwd_balanced_noalloc",
     "Workspace",
     "xs_attn_get_device_error",
     "xs_attn_error_string",
@@ -74,6 +75,8 @@ EXPORTS = {
     "xs_attn_workspace_bytes": (_int, [_int, _int, _int, _int, ctypes.POINTER(_size)]),
     "xs_attn_fwd_balanced": (_int, [_vp, _vp, _vp, _int, ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32,
                                     _vp, _size, _vp]),
+    "xs_attn_fwd_balanced_noalloc": (_int, [_vp, _vp, _vp, _int, ctypes.POINTER(_vp), _int, _int, _int, _int, _int,
+                                            _f32, _vp]),
     "xs_attn_get_device_error": (_int, [_vp]),
     "xs_attn_error_string": (ctypes.c_char_p, [_int]),
     "xs_attn_last_cuda_error": (_int, []),
@@ -232,6 +235,17 @@ def xs_attn_get_device_error(stream=None) -> int:
 
 def xs_attn_error_string(code: int) -> str:
     return lib.xs_attn_error_string(code).decode()
+
+
+def xs_attn_fwd_balanced_noalloc(q, k, v, layout: int, outs, scale: float, stream=None) -> None:
+    """:func:`xs_attn_fwd_balanced` with the library's own scratch array as workspace (no
+    allocation on the call path; calls that overlap in time race on the one array)."""
+    B, S, H, D = _bshd(q, "q").shape
+    _bshd(k, "k"), _bshd(v, "v")
+    os_ = [_bshd(o, "out") for o in outs]
+    _check(lib.xs_attn_fwd_balanced_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), layout,
+                                            _ptr_array([o.data_ptr() for o in os_]), B, S, H, D, len(os_), scale,
+                                            _stream_handle(stream)), "xs_attn_fwd_balanced_noalloc")
 
 
 def attn_a2a(q, k, v, P: int, scale: float | None = None, stream=None, workspace=None):

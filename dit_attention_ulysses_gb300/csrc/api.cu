@@ -351,6 +351,38 @@ int attn_layout_call(const void* q, const void* k, const void* v, int layout, vo
     return run_attention(q, k, v, epi, B, S, H, D, scale, ws, ws_bytes, stream);
 }
 
+// ---- scratch of xs_attn_fwd_balanced_noalloc
+// Callers that may not allocate device memory on their call path (a serving
+// loop that reserves all memory at start-up and forbids allocation afterwards:
+// cudaMalloc can fail there, and cudaFree synchronises the whole device) get the
+// balanced schedule's workspace from this file-scope array instead of from a
+// buffer of their own.  It is zero-filled when the module is loaded, which is
+// all the split-tile flags need (a zero flag never matches a launch epoch).
+// 11 MiB covers the largest workspace the schedule asks for on a 152-SM GB300
+// (D = 128: 152 slots x 66,592 B ~ 10.1 MB); a larger need is refused with
+// XS_ERR_WORKSPACE.
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(11) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[MAX_DEVICES] = {};
+
+// Address of this device's copy of g_noalloc_scratch, looked up once per device.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= MAX_DEVICES) return XS_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return XS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -382,6 +414,28 @@ int xs_attn_workspace_bytes(int B, int S, int H, int D, size_t* bytes) {
     if ((rc = device_info(&dev)) != XS_OK) return rc;
     *bytes = make_plan(B, S, H, D, dev).ws_bytes;
     return XS_OK;
+}
+
+int xs_attn_fwd_balanced_noalloc(const void* q, const void* k, const void* v, int layout, void* const* outs, int B,
+                                 int S, int H, int D, int P, float scale, void* stream) {
+    // argument checks first, so that an invalid call touches no CUDA state
+    if (!outs) return XS_ERR_NULL;
+    xs::EpiParams epi;
+    int n_out = 0;
+    int64_t out_bytes = 0;
+    bool need_div = false;
+    int rc = layout_epi(layout, outs, B, S, H, D, P, &epi, &n_out, &out_bytes, &need_div);
+    if (rc != XS_OK) return rc;
+    rc = validate_attn(q, k, v, outs, n_out, B, S, H, D, layout == XS_LAYOUT_CONTIGUOUS ? 1 : P, scale, out_bytes,
+                       need_div);
+    if (rc != XS_OK) return rc;
+    size_t need = 0;
+    if ((rc = xs_attn_workspace_bytes(B, S, H, D, &need)) != XS_OK) return rc;
+    if (need > NOALLOC_SCRATCH_BYTES) return XS_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch)) != XS_OK) return rc;
+    return attn_layout_call(q, k, v, layout, outs, B, S, H, D, P, scale, scratch, NOALLOC_SCRATCH_BYTES,
+                            static_cast<cudaStream_t>(stream));
 }
 
 int xs_attn_fwd_balanced(const void* q, const void* k, const void* v, int layout, void* const* outs, int B, int S,

@@ -189,6 +189,33 @@ int xs_attn_fwd_balanced(const void* q, const void* k, const void* v, int layout
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * xs_attn_fwd_balanced_noalloc -- xs_attn_fwd_balanced with the workspace taken
+ * from a scratch array inside the library instead of from the caller.  The
+ * X-Stage paper has no counterpart to this entry point: it exists for callers
+ * that may not allocate device memory on their call path (for example a serving
+ * loop that reserves all memory at start-up; cudaMalloc may fail there and
+ * cudaFree synchronises the whole device), so that they need not size, allocate
+ * and keep a workspace of their own.
+ *   Scratch: one array of 11 MiB (11,534,336 bytes) per device, a file-scope
+ *   device variable of the library, zero-filled when the library's module is
+ *   loaded; nothing else must start at zero.  A shape whose workspace
+ *   (xs_attn_workspace_bytes) exceeds it gets XS_ERR_WORKSPACE and nothing is
+ *   launched; on a 152-SM GB300 the largest need is about 10.1 MB (D = 128).
+ *   No device or host memory is allocated by the call.
+ *   Setup: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, which may load the library's device code); make that
+ *   first call before any stream capture begins.
+ *   Concurrency: all calls on a device share the one array.  Calls that may run
+ *   at the same time (other streams, other host threads) race on it and give
+ *   wrong results; order them (one stream, or events/synchronisation).
+ * Arguments, outputs, checks and errors are those of xs_attn_fwd_balanced
+ * (without workspace / workspace_bytes); the results are bit-identical to
+ * xs_attn_fwd_balanced's for the same inputs.
+ */
+int xs_attn_fwd_balanced_noalloc(const void* q, const void* k, const void* v, int layout, void* const* outs,
+                                 int B, int S, int H, int D, int P, float scale, void* stream);
+
+/*
  * xs_attn_get_device_error -- synchronises `stream`, then reads and clears the
  * library's device error word on the current device.  Returns XS_OK, or
  * XS_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel expired (the kernel
