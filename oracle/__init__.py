@@ -170,3 +170,32 @@ def attention_a2a(q, k, v, scale: float, P: int, nthreads: int | None = None) ->
     Returns the P output shards as one array [P, B, S/P, H, D] (float64).
     """
     return a2a(head_shards(attention(q, k, v, scale, nthreads), P))
+
+
+def _exact_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float64 values that are exactly bf16 -> their bf16 bit patterns (checked)."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    bits = (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    back = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    if not np.array_equal(back, f):
+        raise ValueError("values are not exactly representable in bf16")
+    return bits
+
+
+def ulysses_attention(q_shards, k_shards, v_shards, scale: float, nthreads: int | None = None) -> np.ndarray:
+    """The Ulysses attention step of P ranks, in its three steps (DeepSpeed-Ulysses
+    sequence parallelism, as used by the X-Stage paper's DiT inference):
+
+    1. pre-attention All-to-All: rank p's sequence shard [B,S/P,H,D] of each of Q, K, V
+       is exchanged so that rank r holds all S rows of heads [r*H/P, (r+1)*H/P);
+    2. every rank runs exact attention on its own heads;
+    3. post-attention All-to-All back to sequence shards.
+
+    q_shards etc.: [P, B, S/P, H, D] bf16 bits (uint16).  Returns [P, B, S/P, H, D] float64.
+    """
+    widen = lambda b: (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(
+        np.float32).astype(np.float64)
+    Lq, Lk, Lv = (a2a_inverse(widen(x)) for x in (q_shards, k_shards, v_shards))
+    O = np.stack([attention(_exact_bf16_bits(Lq[r]), _exact_bf16_bits(Lk[r]), _exact_bf16_bits(Lv[r]), scale,
+                            nthreads) for r in range(Lq.shape[0])])
+    return a2a(O)

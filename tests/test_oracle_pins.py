@@ -274,3 +274,35 @@ def test_argument_errors():
         oracle.head_shards(o, 2)          # H % P != 0
     with pytest.raises(TypeError):
         oracle.attention(np.zeros((1, 2, 1, 2), np.float32), *[np.zeros((1, 2, 1, 2), np.uint16)] * 2, 1.0)
+
+
+# ------------------------------------------------------------ Ulysses step
+@pytest.mark.parametrize("B,S,H,D,P", [(2, 16, 4, 8, 2), (1, 24, 8, 4, 4), (1, 9, 3, 8, 3)])
+def test_ulysses_step_equals_attention_on_the_whole_sequence(B, S, H, D, P):
+    """The three-step Ulysses oracle (pre-attention exchange, per-rank attention on
+    its heads, post-attention exchange) against brute force on the whole sequence,
+    re-sharded by plain slicing: sequence shard p holds rows [p*S/P, (p+1)*S/P)
+    of every head."""
+    q, k, v = (_rand((B, S, H, D), seed) for seed in (31, 32, 33))
+    Sl = S // P
+    shards = [np.stack([x[:, p * Sl:(p + 1) * Sl] for p in range(P)]) for x in (q, k, v)]
+    got = oracle.ulysses_attention(*shards, 0.7)
+    full = _brute_numpy(q, k, v, 0.7)
+    want = np.stack([full[:, p * Sl:(p + 1) * Sl] for p in range(P)])
+    assert got.shape == (P, B, Sl, H, D)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_ulysses_step_shard_order_equivariance_and_key_value_pairing():
+    """Renumbering the ranks (the same shard order for Q, K and V) renumbers the
+    output shards; giving K alone a different order breaks the key/value pairing
+    and must change the result."""
+    B, S, H, D, P = 1, 16, 4, 8, 4
+    q, k, v = (_rand((B, S, H, D), seed) for seed in (41, 42, 43))
+    Sl = S // P
+    shards = [np.stack([x[:, p * Sl:(p + 1) * Sl] for p in range(P)]) for x in (q, k, v)]
+    good = oracle.ulysses_attention(*shards, 0.5)
+    rev = oracle.ulysses_attention(*[x[::-1].copy() for x in shards], 0.5)
+    np.testing.assert_allclose(rev[::-1], good, rtol=1e-12, atol=1e-12)
+    k_only = oracle.ulysses_attention(shards[0], shards[1][::-1].copy(), shards[2], 0.5)
+    assert np.abs(k_only - good).max() > 1e-3
