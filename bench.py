@@ -264,6 +264,28 @@ def run_ours(args, rank, world, local_rank):
         xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_HEADS, heads, w.scale, ws, stream)
         xs.xs_relayout_a2a(heads, serial, stream)
 
+    # the whole Ulysses step with the inputs as P sequence shards (both exchanges
+    # fused), and its unfused form: pre-attention re-layout of Q, K, V, attention of
+    # each rank on its head shard, post-attention re-layout
+    Sl, Hl = S // P, H // P
+    uly = Sl % 128 == 0
+    if uly:
+        q_sh, k_sh, v_sh = ([X[:, p * Sl:(p + 1) * Sl].contiguous() for p in range(P)] for X in (q, k, v))
+        uly_out = [torch.empty(shard_shape, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        pre = [[torch.empty((B, S, Hl, D), dtype=torch.bfloat16, device=dev) for _ in range(P)] for _ in range(3)]
+        o_heads = [torch.empty((B, S, Hl, D), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        uly_serial = [torch.empty(shard_shape, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+
+        def ulysses_fused():
+            xs.xs_attn_ulysses_fwd(q_sh, k_sh, v_sh, uly_out, w.scale, ws, stream)
+
+        def ulysses_serial():
+            for src, dst in zip((q_sh, k_sh, v_sh), pre):
+                xs.xs_relayout_a2a_inverse(src, dst, stream)
+            for r in range(P):
+                xs.xs_attn_fwd(pre[0][r], pre[1][r], pre[2][r], o_heads[r], w.scale, stream)
+            xs.xs_relayout_a2a(o_heads, uly_serial, stream)
+
     for _ in range(max(3, args.warmup)):
         fused()
     torch.cuda.synchronize()
@@ -294,15 +316,26 @@ def run_ours(args, rank, world, local_rank):
     # ablation: attention alone (contiguous store), fused, and attention + separate
     # re-layout, interleaved run by run so that clock drift affects all three alike
     n_abl = max(10, min(args.steps, 50))
-    for fn in (alone, serial_path):
+    for fn in (alone, serial_path) + ((ulysses_fused, ulysses_serial) if uly else ()):
         for _ in range(3):
             fn()
-    ta, tf, ts = [], [], []
+    ta, tf, ts, tuf, tus = [], [], [], [], []
     for _ in range(n_abl):
         ta += time_steps(torch, alone, 1, flush, stream)
         tf += time_steps(torch, fused, 1, flush, stream)
         ts += time_steps(torch, serial_path, 1, flush, stream)
+        if uly:
+            tuf += time_steps(torch, ulysses_fused, 1, flush, stream)
+            tus += time_steps(torch, ulysses_serial, 1, flush, stream)
     t_alone, t_fused, t_serial = statistics.median(ta), statistics.median(tf), statistics.median(ts)
+    ulysses = None
+    if uly:
+        t_uf, t_us = statistics.median(tuf), statistics.median(tus)
+        ulysses = {"api": "xs_attn_ulysses_fwd", "fused_step_ms": t_uf, "fused_step_tflops": w.flops / (t_uf * 1e-3) / 1e12,
+                   "unfused_step_ms": t_us, "unfused_over_fused": t_us / t_uf,
+                   "fused_step_over_whole_tensor_fused": t_uf / t_fused,
+                   "unfused": "pre-attention re-layout of Q, K, V + attention per rank + post-attention re-layout",
+                   "runs": n_abl, "statistic": "median"}
 
     # end to end through the host-buffer entry point: H2D of q, k, v, kernel, D2H of the shards
     pin = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -350,6 +383,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": whole_job_tflops(w.flops, e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 3 * w.tensor_bytes, "d2h_bytes_per_step": w.tensor_bytes,
                 "ms_per_step": e2e_ms, "api": "xs_attn_a2a_fwd_staged"},
+        "ulysses_step": ulysses,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),

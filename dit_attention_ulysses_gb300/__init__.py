@@ -25,6 +25,8 @@ __all__ = [
     "xs_attn_fwd",
     "xs_attn_heads_fwd",
     "xs_relayout_a2a",
+    "xs_relayout_a2a_inverse",
+    "xs_attn_ulysses_fwd",
     "xs_attn_a2a_fwd_staged",
     "xs_attn_workspace_bytes",
     "xs_attn_fwd_balanced",
@@ -77,6 +79,10 @@ EXPORTS = {
                                     _vp, _size, _vp]),
     "xs_attn_fwd_balanced_noalloc": (_int, [_vp, _vp, _vp, _int, ctypes.POINTER(_vp), _int, _int, _int, _int, _int,
                                             _f32, _vp]),
+    "xs_attn_ulysses_fwd": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                   ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32, _vp, _size, _vp]),
+    "xs_relayout_a2a_inverse": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int, _int, _int, _int,
+                                       _vp]),
     "xs_attn_get_device_error": (_int, [_vp]),
     "xs_attn_error_string": (ctypes.c_char_p, [_int]),
     "xs_attn_last_cuda_error": (_int, []),
@@ -169,6 +175,32 @@ def xs_relayout_a2a(heads, out_ptrs, stream=None) -> None:
     B, S, Hl, D = hs[0].shape
     _check(lib.xs_relayout_a2a(_ptr_array([x.data_ptr() for x in hs]), _ptr_array([o.data_ptr() for o in outs]),
                                B, S, Hl * P, D, P, _stream_handle(stream)), "xs_relayout_a2a")
+
+
+def xs_attn_ulysses_fwd(q_shards, k_shards, v_shards, out_shards, scale: float, workspace=None,
+                        stream=None) -> None:
+    """The Ulysses attention step of P virtual ranks in one launch: inputs are the P sequence
+    shards [B,S/P,H,D] of Q, K and V, outputs the P sequence shards [B,S/P,H,D] of O."""
+    qs = [_bshd(x, "q_shards") for x in q_shards]
+    ks = [_bshd(x, "k_shards") for x in k_shards]
+    vs = [_bshd(x, "v_shards") for x in v_shards]
+    os_ = [_bshd(x, "out_shards") for x in out_shards]
+    P = len(qs)
+    B, Sl, H, D = qs[0].shape
+    wp, wn = _ws(workspace)
+    _check(lib.xs_attn_ulysses_fwd(_ptr_array([x.data_ptr() for x in qs]), _ptr_array([x.data_ptr() for x in ks]),
+                                   _ptr_array([x.data_ptr() for x in vs]), _ptr_array([x.data_ptr() for x in os_]),
+                                   B, Sl * P, H, D, P, scale, wp, wn, _stream_handle(stream)), "xs_attn_ulysses_fwd")
+
+
+def xs_relayout_a2a_inverse(seq_shards, heads, stream=None) -> None:
+    """Separate pre-attention All-to-All: sequence shards [B,S/P,H,D] -> head shards [B,S,H/P,D]."""
+    ss = [_bshd(x, "seq_shards") for x in seq_shards]
+    hs = [_bshd(x, "heads") for x in heads]
+    P = len(ss)
+    B, Sl, H, D = ss[0].shape
+    _check(lib.xs_relayout_a2a_inverse(_ptr_array([x.data_ptr() for x in ss]), _ptr_array([x.data_ptr() for x in hs]),
+                                       B, Sl * P, H, D, P, _stream_handle(stream)), "xs_relayout_a2a_inverse")
 
 
 def xs_attn_a2a_fwd_staged(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, scale: float,

@@ -244,18 +244,18 @@ unsigned next_epoch() {
 
 // ws == nullptr: plain schedule.  Otherwise the balanced schedule whenever it
 // splits tiles; ws must then hold plan.ws_bytes bytes (256-byte aligned).
-int run_attention(const void* q, const void* k, const void* v, const xs::EpiParams& epi, int B, int S, int H, int D,
-                  float scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+// Inputs: q, k, v each one [B,S,H,D] tensor, or (shards != nullptr) the P
+// sequence shards [B,S/P,H,D] of each operand: shards[0..P) = q, [P..2P) = k,
+// [2P..3P) = v, with (S/P) % 128 == 0.
+int run_attention(const void* q, const void* k, const void* v, const void* const* shards, int P,
+                  const xs::EpiParams& epi, int B, int S, int H, int D, float scale, void* ws, size_t ws_bytes,
+                  cudaStream_t stream) {
     DeviceInfo dev;
     int rc = device_info(&dev);
     if (rc != XS_OK) return rc;
     const Plan pl = make_plan(B, S, H, D, dev);
     const bool split = ws != nullptr && pl.split;
     if (split && ws_bytes < pl.ws_bytes) return XS_ERR_WORKSPACE;
-    CUtensorMap tq, tk, tv;
-    if ((rc = encode_bshd(&tq, q, B, S, H, D)) != XS_OK) return rc;
-    if ((rc = encode_bshd(&tk, k, B, S, H, D)) != XS_OK) return rc;
-    if ((rc = encode_bshd(&tv, v, B, S, H, D)) != XS_OK) return rc;
     xs::AttnArgs a;
     std::memset(&a, 0, sizeof a);
     a.B = B;
@@ -281,8 +281,27 @@ int run_attention(const void* q, const void* k, const void* v, const xs::EpiPara
         a.sp.dp_tiles = a.units;
         grid = a.units < dev.sms ? a.units : dev.sms;
     }
-    cudaError_t e = (D == 128) ? xs::launch_attn<128>(tq, tk, tv, a, grid, split, stream)
-                               : xs::launch_attn<64>(tq, tk, tv, a, grid, split, stream);
+    cudaError_t e;
+    if (shards) {
+        static thread_local xs::ShardMaps maps;   // 6 KB: kept off the stack
+        const int Sl = S / P;
+        for (int p = 0; p < P; ++p) {
+            if ((rc = encode_bshd(&maps.q[p], shards[p], B, Sl, H, D)) != XS_OK) return rc;
+            if ((rc = encode_bshd(&maps.k[p], shards[P + p], B, Sl, H, D)) != XS_OK) return rc;
+            if ((rc = encode_bshd(&maps.v[p], shards[2 * P + p], B, Sl, H, D)) != XS_OK) return rc;
+        }
+        a.in_Sl = Sl;
+        a.in_inv_Sl = 1.0f / static_cast<float>(Sl);
+        e = (D == 128) ? xs::launch_attn_sharded<128>(maps, P, a, grid, split, stream)
+                       : xs::launch_attn_sharded<64>(maps, P, a, grid, split, stream);
+    } else {
+        CUtensorMap tq, tk, tv;
+        if ((rc = encode_bshd(&tq, q, B, S, H, D)) != XS_OK) return rc;
+        if ((rc = encode_bshd(&tk, k, B, S, H, D)) != XS_OK) return rc;
+        if ((rc = encode_bshd(&tv, v, B, S, H, D)) != XS_OK) return rc;
+        e = (D == 128) ? xs::launch_attn<128>(tq, tk, tv, a, grid, split, stream)
+                       : xs::launch_attn<64>(tq, tk, tv, a, grid, split, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return XS_OK;
 }
@@ -348,7 +367,7 @@ int attn_layout_call(const void* q, const void* k, const void* v, int layout, vo
                        need_div);
     if (rc != XS_OK) return rc;
     if ((rc = check_workspace(ws, ws_bytes, q, k, v, outs, n_out, out_bytes, B, S, H, D)) != XS_OK) return rc;
-    return run_attention(q, k, v, epi, B, S, H, D, scale, ws, ws_bytes, stream);
+    return run_attention(q, k, v, nullptr, 0, epi, B, S, H, D, scale, ws, ws_bytes, stream);
 }
 
 // ---- scratch of xs_attn_fwd_balanced_noalloc
@@ -436,6 +455,81 @@ int xs_attn_fwd_balanced_noalloc(const void* q, const void* k, const void* v, in
     if ((rc = noalloc_scratch(&scratch)) != XS_OK) return rc;
     return attn_layout_call(q, k, v, layout, outs, B, S, H, D, P, scale, scratch, NOALLOC_SCRATCH_BYTES,
                             static_cast<cudaStream_t>(stream));
+}
+
+int xs_attn_ulysses_fwd(const void* const* q_shards, const void* const* k_shards, const void* const* v_shards,
+                        void* const* out_shards, int B, int S, int H, int D, int P, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    if (!q_shards || !k_shards || !v_shards || !out_shards) return XS_ERR_NULL;
+    int rc = check_shape(B, S, H, D, P, true);
+    if (rc != XS_OK) return rc;
+    const int Sl = S / P;
+    if (Sl % 128 != 0) return XS_ERR_DIVISIBILITY;
+    const void* in[3 * XS_MAX_P];
+    for (int p = 0; p < P; ++p) {
+        in[p] = q_shards[p];
+        in[P + p] = k_shards[p];
+        in[2 * P + p] = v_shards[p];
+    }
+    for (int i = 0; i < 3 * P; ++i)
+        if (!in[i]) return XS_ERR_NULL;
+    for (int p = 0; p < P; ++p)
+        if (!out_shards[p]) return XS_ERR_NULL;
+    if ((rc = check_scale(scale)) != XS_OK) return rc;
+    for (int i = 0; i < 3 * P; ++i)
+        if (!aligned16(in[i])) return XS_ERR_ALIGNMENT;
+    for (int p = 0; p < P; ++p)
+        if (!aligned16(out_shards[p])) return XS_ERR_ALIGNMENT;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return XS_ERR_ALIGNMENT;
+    const int64_t shard_bytes = static_cast<int64_t>(B) * Sl * H * D * 2;
+    Range ins[3 * XS_MAX_P + 1], outs[XS_MAX_P + 1];
+    for (int i = 0; i < 3 * P; ++i) ins[i] = range_of(in[i], shard_bytes);
+    for (int p = 0; p < P; ++p) outs[p] = range_of(out_shards[p], shard_bytes);
+    int n_out = P;
+    if (workspace) outs[n_out++] = range_of(workspace, static_cast<int64_t>(workspace_bytes));
+    if ((rc = check_disjoint(outs, n_out, ins, 3 * P)) != XS_OK) return rc;
+    xs::EpiParams epi;
+    std::memset(&epi, 0, sizeof epi);
+    for (int p = 0; p < P; ++p) epi.ptr[p] = out_shards[p];
+    epi.Sl = Sl;
+    epi.Hl = H;
+    return run_attention(nullptr, nullptr, nullptr, in, P, epi, B, S, H, D, scale, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int xs_relayout_a2a_inverse(const void* const* seq_shards, void* const* heads, int B, int S, int H, int D, int P,
+                            void* stream) {
+    if (!seq_shards || !heads) return XS_ERR_NULL;
+    int rc = check_shape(B, S, H, D, P, true);
+    if (rc != XS_OK) return rc;
+    for (int p = 0; p < P; ++p)
+        if (!seq_shards[p] || !heads[p]) return XS_ERR_NULL;
+    for (int p = 0; p < P; ++p)
+        if (!aligned16(seq_shards[p]) || !aligned16(heads[p])) return XS_ERR_ALIGNMENT;
+    const int64_t head_bytes = static_cast<int64_t>(B) * S * (H / P) * D * 2;
+    const int64_t shard_bytes = static_cast<int64_t>(B) * (S / P) * H * D * 2;
+    Range ins[XS_MAX_P], outs[XS_MAX_P];
+    for (int p = 0; p < P; ++p) {
+        ins[p] = range_of(seq_shards[p], shard_bytes);
+        outs[p] = range_of(heads[p], head_bytes);
+    }
+    if ((rc = check_disjoint(outs, P, ins, P)) != XS_OK) return rc;
+    DeviceInfo dev;
+    if ((rc = device_info(&dev)) != XS_OK) return rc;
+    xs::RelayoutArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int p = 0; p < P; ++p) {
+        a.heads[p] = seq_shards[p];   // inverse direction: read sequence shards,
+        a.out[p] = heads[p];          // write head shards
+    }
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.D = D;
+    a.P = P;
+    cudaError_t e = xs::launch_relayout_inverse(a, dev.sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return XS_OK;
 }
 
 int xs_attn_fwd_balanced(const void* q, const void* k, const void* v, int layout, void* const* outs, int B, int S,

@@ -247,6 +247,26 @@ __device__ __forceinline__ void ring_item(int i, int n, int& blk, bool& is_v) {
 }
 
 // ---------------------------------------------------------------- producer
+// Tensor map and row coordinate of sequence row `row` (a multiple of 128): one
+// map for the whole tensor, or, for sequence-sharded inputs, the map of shard
+// row / in_Sl and the row within it (a tile never straddles two shards because
+// in_Sl is a multiple of 128).
+__device__ __forceinline__ const CUtensorMap* pick_map(const AttnArgs& a, const CUtensorMap* maps, int row,
+                                                      int& row_in_map) {
+    if (a.in_Sl == 0) {
+        row_in_map = row;
+        return maps;
+    }
+    // No integer division: this runs in the single producer thread, whose
+    // instruction latency is on the pipeline's critical path.  The fp32 estimate
+    // is off by at most one shard; the two corrections make it exact.
+    int p = __float2int_rz(__int2float_rn(row) * a.in_inv_Sl);
+    if (p * a.in_Sl > row) --p;
+    if ((p + 1) * a.in_Sl <= row) ++p;
+    row_in_map = row - p * a.in_Sl;
+    return maps + p;
+}
+
 // Run by one thread.
 template <int D>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
@@ -266,15 +286,20 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
             ok = thread_wait(bar(C::B_Q_FREE + qb), ((u_iter / C::Q_BUFS) - 1) & 1, abort_flag, a.timeout_ns);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(C::B_Q_FULL + qb), C::TILE_BYTES);
+        int q_row;
+        const CUtensorMap* q_map = pick_map(a, tq, qt * BLOCK_M, q_row);
         for (int pnl = 0; pnl < C::PANELS; ++pnl)
-            tma_load_4d(sbase + C::Q_OFF + qb * C::TILE_BYTES + pnl * PANEL_BYTES, tq, bar(C::B_Q_FULL + qb),
-                        pnl * 64, h, qt * BLOCK_M, b);
+            tma_load_4d(sbase + C::Q_OFF + qb * C::TILE_BYTES + pnl * PANEL_BYTES, q_map, bar(C::B_Q_FULL + qb),
+                        pnl * 64, h, q_row, b);
         q_last = u_iter;
         {   // start the next piece's Q towards L2: its load waits for this piece's
             // last S MMA (one Q buffer at D = 128) and then hits L2, not HBM
             Work wn;
-            if (get_work(a, u_iter + 1, wn))
-                for (int pnl = 0; pnl < C::PANELS; ++pnl) tma_prefetch_l2_4d(tq, pnl * 64, wn.h, wn.qt * BLOCK_M, wn.b);
+            if (get_work(a, u_iter + 1, wn)) {
+                int r;
+                const CUtensorMap* m = pick_map(a, tq, wn.qt * BLOCK_M, r);
+                for (int pnl = 0; pnl < C::PANELS; ++pnl) tma_prefetch_l2_4d(m, pnl * 64, wn.h, r, wn.b);
+            }
         }
         for (int i = 0; i < 2 * w.nb && ok; ++i) {
             int blk;
@@ -286,9 +311,11 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
             if (round > 0) ok = thread_wait(bar(C::B_KV_FREE + stage), (round - 1) & 1, abort_flag, a.timeout_ns);
             if (!ok) break;
             mbar_arrive_expect_tx(bar(C::B_KV_FULL + stage), C::TILE_BYTES);
+            int kv_row;
+            const CUtensorMap* kv_map = pick_map(a, is_v ? tv : tk, blk * BLOCK_N, kv_row);
             for (int pnl = 0; pnl < C::PANELS; ++pnl)
-                tma_load_4d(sbase + C::KV_OFF + stage * C::TILE_BYTES + pnl * PANEL_BYTES, is_v ? tv : tk,
-                            bar(C::B_KV_FULL + stage), pnl * 64, h, blk * BLOCK_N, b);
+                tma_load_4d(sbase + C::KV_OFF + stage * C::TILE_BYTES + pnl * PANEL_BYTES, kv_map,
+                            bar(C::B_KV_FULL + stage), pnl * 64, h, kv_row, b);
             ++item;
         }
     }
@@ -719,10 +746,11 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
     }
 }
 
+// The whole kernel; tq, tk, tv point to one tensor map each, or to n_maps maps
+// (one per input sequence shard, args.in_Sl != 0).
 template <int D>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    attn_a2a_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ AttnArgs args) {
+__device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                          int n_maps, const AttnArgs& args) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -751,10 +779,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == WARP_TMA && lane_id() == 0) {
-        tma_prefetch_desc(&tmap_q);
-        tma_prefetch_desc(&tmap_k);
-        tma_prefetch_desc(&tmap_v);
+    if (warp == WARP_TMA && lane_id() < n_maps) {
+        tma_prefetch_desc(tq + lane_id());
+        tma_prefetch_desc(tk + lane_id());
+        tma_prefetch_desc(tv + lane_id());
     }
     if (warp == WARP_MMA_S) {
         tmem_alloc(smem_addr(tmem_holder), TMEM_COLS);
@@ -770,7 +798,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (lane_id() == 0) {
         // single-thread roles; the other lanes of these warps wait at the end
         if (warp == WARP_TMA)
-            producer_role<D>(&tmap_q, &tmap_k, &tmap_v, args, smem, bar0, abort_flag);
+            producer_role<D>(tq, tk, tv, args, smem, bar0, abort_flag);
         else if (warp == WARP_MMA_S)
             mma_s_role<D>(args, smem, bar0, tmem_base, abort_flag);
         else
@@ -782,6 +810,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == WARP_MMA_S) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_a2a_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ AttnArgs args) {
+    attn_body<D>(&tmap_q, &tmap_k, &tmap_v, 1, args);
+}
+
+// Q, K, V read straight from the P sequence shards of the Ulysses ranks: the
+// pre-attention All-to-All is fused into the loads (each tile's TMA box comes
+// from the shard that holds its rows), as the post-attention one is into the
+// epilogue stores.
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_ulysses_kernel(const __grid_constant__ AttnArgs args, const __grid_constant__ ShardMaps maps) {
+    attn_body<D>(maps.q, maps.k, maps.v, args.S / args.in_Sl, args);
 }
 
 }  // namespace
@@ -813,6 +858,26 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                                        Cfg<D>::SMEM_ALLOC, stream);
 }
 
+template <int D>
+cudaError_t launch_attn_sharded(const ShardMaps& maps, int P, const AttnArgs& args, int grid, bool cooperative,
+                                cudaStream_t stream) {
+    (void)P;
+    auto kern = attn_ulysses_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    if (!cooperative) {
+        kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(args, maps);
+        return cudaGetLastError();
+    }
+    ShardMaps m = maps;
+    AttnArgs a = args;
+    void* params[] = {&a, &m};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(NUM_THREADS), params,
+                                       Cfg<D>::SMEM_ALLOC, stream);
+}
+
+template cudaError_t launch_attn_sharded<64>(const ShardMaps&, int, const AttnArgs&, int, bool, cudaStream_t);
+template cudaError_t launch_attn_sharded<128>(const ShardMaps&, int, const AttnArgs&, int, bool, cudaStream_t);
 template int attn_smem_bytes<64>();
 template int attn_smem_bytes<128>();
 template cudaError_t launch_attn<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const AttnArgs&, int,

@@ -52,6 +52,17 @@ struct AttnArgs {
     EpiParams epi;
     unsigned long long timeout_ns;  // limit for every wait inside the kernel
     SplitParams sp;
+    int in_Sl;      // inputs as sequence shards: rows per shard (a multiple of 128);
+                    // 0: one [B, S, H, D] tensor per operand
+    float in_inv_Sl;  // 1 / in_Sl (fp32), for a division-free shard lookup
+};
+
+// Tensor maps of Q, K, V given as P sequence shards [B, S/P, H, D] each (the
+// layout every Ulysses rank holds before the pre-attention All-to-All).
+struct ShardMaps {
+    CUtensorMap q[MAX_PTRS];
+    CUtensorMap k[MAX_PTRS];
+    CUtensorMap v[MAX_PTRS];
 };
 
 template <int D>
@@ -63,6 +74,11 @@ template <int D>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnArgs& args, int grid, bool cooperative, cudaStream_t stream);
 
+// The same kernel reading Q, K, V from P sequence shards (args.in_Sl = S / P).
+template <int D>
+cudaError_t launch_attn_sharded(const ShardMaps& maps, int P, const AttnArgs& args, int grid, bool cooperative,
+                                cudaStream_t stream);
+
 cudaError_t read_and_clear_device_error(int* value);
 
 struct RelayoutArgs {
@@ -72,5 +88,10 @@ struct RelayoutArgs {
 };
 
 cudaError_t launch_relayout(const RelayoutArgs& a, int num_sms, cudaStream_t stream);
+
+// The inverse exchange (the pre-attention All-to-All): a.heads[p] are read as the
+// sequence shards [B, S/P, H, D], a.out[r] are written as the head shards
+// [B, S, H/P, D].
+cudaError_t launch_relayout_inverse(const RelayoutArgs& a, int num_sms, cudaStream_t stream);
 
 }  // namespace xs

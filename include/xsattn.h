@@ -126,6 +126,49 @@ int xs_relayout_a2a(const void* const* heads, void* const* out_ptrs,
                     int B, int S, int H, int D, int P, void* stream);
 
 /*
+ * xs_attn_ulysses_fwd -- the whole Ulysses attention step of P virtual ranks in
+ * one launch, both exchanges fused.  Ulysses (DeepSpeed-Ulysses, the sequence
+ * parallelism the X-Stage paper's DiT inference uses) gives every rank a
+ * sequence shard of Q, K and V; a pre-attention All-to-All turns them into head
+ * shards (all S rows of H/P heads), every rank runs attention on its heads, and
+ * the post-attention All-to-All returns sequence shards.  Here the kernel loads
+ * each Q tile and each K/V block straight from the sequence shard that holds its
+ * rows (one TMA tensor map per shard), so the pre-attention exchange becomes the
+ * loads, and stores the output as xs_attn_a2a_fwd does, so the post-attention
+ * exchange becomes the stores.  The X-Stage summary ("Key Contributions" item 3)
+ * fuses only the post-attention exchange; fusing the pre-attention one into the
+ * loads is this library's extension of the same idea.
+ *   q_shards, k_shards, v_shards  host arrays of P device pointers, shard p a
+ *             [B, S/P, H, D] bf16 buffer holding sequence rows [p*S/P, (p+1)*S/P);
+ *             read only (they may alias each other).
+ *   out_shards host array of P device pointers, [B, S/P, H, D] bf16 each, the
+ *             layout of xs_attn_a2a_fwd; must not overlap any input, each other
+ *             or the workspace.
+ *   P         1 <= P <= XS_MAX_P, H % P == 0 and (S/P) % 128 == 0 (a 128-row
+ *             tile must lie in one shard), else XS_ERR_DIVISIBILITY.
+ *   workspace, workspace_bytes  as in xs_attn_fwd_balanced (NULL, 0: whole
+ *             tiles only).
+ * Arithmetic identical to xs_attn_a2a_fwd on the concatenated inputs: the
+ * outputs are bit-identical to it for the same schedule.
+ */
+int xs_attn_ulysses_fwd(const void* const* q_shards, const void* const* k_shards, const void* const* v_shards,
+                        void* const* out_shards, int B, int S, int H, int D, int P, float scale,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * xs_relayout_a2a_inverse -- the separate pre-attention All-to-All re-layout
+ * (single GPU), the inverse of xs_relayout_a2a:
+ *     heads[r][b, s, j, :] = seq_shards[s / (S/P)][b, s % (S/P), r*(H/P) + j, :]
+ * seq_shards: host array of P device pointers to [B,S/P,H,D] bf16 buffers;
+ * heads: host array of P device pointers to [B,S,H/P,D] bf16 buffers.  Outputs
+ * must not overlap the inputs or each other.  Pure data movement; bit-exact.
+ * With xs_attn_fwd (per rank) and xs_relayout_a2a it forms the unfused Ulysses
+ * step that xs_attn_ulysses_fwd is measured against.
+ */
+int xs_relayout_a2a_inverse(const void* const* seq_shards, void* const* heads,
+                            int B, int S, int H, int D, int P, void* stream);
+
+/*
  * xs_attn_a2a_fwd_staged -- xs_attn_a2a_fwd for host-resident data.
  * Copies q, k, v from host memory (pinned for asynchronous copies) into the
  * caller's device buffers q_dev, k_dev, v_dev, runs the fused kernel into the

@@ -169,3 +169,24 @@ def test_python_binding_rejects_cpu_tensors(xs):
     q = torch.zeros(1, 256, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         xs.xs_attn_a2a_fwd(q, q, q, [q, q], 0.125)
+
+
+def test_ulysses_and_inverse_relayout_validation(xs):
+    lib = xs.lib
+    qs, ks, vs = _outs(2, base=0x10_0000_0000), _outs(2, base=0x20_0000_0000), _outs(2, base=0x30_0000_0000)
+    outs = _outs(2)
+    # (S/P) % 128 != 0: a tile would straddle two input shards
+    assert lib.xs_attn_ulysses_fwd(qs, ks, vs, outs, 1, 384, 2, 64, 2, 0.1, None, 0, None) == xs.XS_ERR_DIVISIBILITY
+    assert lib.xs_attn_ulysses_fwd(qs, ks, vs, outs, 1, 512, 3, 64, 2, 0.1, None, 0, None) == xs.XS_ERR_DIVISIBILITY
+    assert lib.xs_attn_ulysses_fwd(None, ks, vs, outs, 1, 512, 2, 64, 2, 0.1, None, 0, None) == xs.XS_ERR_NULL
+    # an output shard inside an input shard
+    assert lib.xs_attn_ulysses_fwd(qs, ks, vs, _outs(2, base=0x20_0000_0000 + 4096), 1, 512, 2, 64, 2, 0.1,
+                                   None, 0, None) == xs.XS_ERR_OVERLAP
+    # the workspace inside an output shard
+    assert lib.xs_attn_ulysses_fwd(qs, ks, vs, outs, 1, 512, 2, 64, 2, 0.1, outs[0], 1 << 20, None) == \
+        xs.XS_ERR_OVERLAP
+    assert lib.xs_attn_ulysses_fwd(qs, ks, vs, outs, 1, 512, 2, 64, 2, 0.1, 0x60_0000_0010, 1 << 20, None) == \
+        xs.XS_ERR_ALIGNMENT
+    assert lib.xs_relayout_a2a_inverse(qs, outs, 1, 256, 3, 64, 2, None) == xs.XS_ERR_DIVISIBILITY
+    assert lib.xs_relayout_a2a_inverse(qs, _outs(2, base=0x10_0000_0000 + 4096), 1, 256, 2, 64, 2, None) == \
+        xs.XS_ERR_OVERLAP
