@@ -8,21 +8,31 @@
 // P device buffers, so the "remote store" is a 16-byte vector store into the
 // owner's [B, S/P, H, D] shard.
 //
-// Kernel organisation (one persistent CTA per SM, 11 warps):
+// Kernel organisation (one persistent CTA per SM, 12 warps; warp w runs on SM
+// sub-partition w % 4):
 //   warps 0-7  softmax + epilogue of the current 128-row Q tile; two threads per
 //              row: warp w owns rows 32*(w%4) .. +31 (its TMEM lane quarter) and
 //              key columns 64*(w/4) .. +63 of every score block
-//   warp  8    TMA producer: Q tile of each work unit, then the K/V ring in
-//              consumption order K0, K1, V0, K2, V1, K3, ...  (D = 128: one Q
-//              buffer, reloaded as soon as the unit's last S MMA has read it;
-//              D = 64: two Q buffers)
+//   warp  8    idle (keeps the three single-thread roles on three different
+//              sub-partitions without changing the register budget: at most
+//              three warps per sub-partition either way)
 //   warp  9    issuer of the S = Q K^T MMAs (one lane) and TMEM owner
 //   warp 10    issuer of the O += P V MMAs (one lane)
+//   warp 11    TMA producer (one lane): Q tile of each piece of work, then the
+//              K/V ring in consumption order K0, K1, V0, K2, V1, K3, ...
+//              (D = 128: one Q buffer, reloaded as soon as the piece's last S MMA
+//              has read it, the next one prefetched into L2 meanwhile; D = 64:
+//              two Q buffers)
 // The tcgen05 issue queue is shallow, so any control work an issuing thread
 // does between MMAs (waits, commits) leaves the tensor core idle; with two
-// issuers, one thread's control work overlaps the other thread's MMAs.
-// A work unit is (b, h, 128 query rows), numbered head-major so that the CTAs
-// running at the same time share K/V through L2.
+// issuers, one thread's control work overlaps the other thread's MMAs.  The
+// single-thread roles share their sub-partitions with softmax warps, so their
+// instruction latency matters: sharing one sub-partition between two of them
+// measured 1-2 % slower.
+// A tile is (b, h, 128 query rows), numbered head-major so that the CTAs running
+// at the same time share K/V through L2.  Q, K, V come from one [B,S,H,D]
+// tensor each, or from the P sequence shards of the Ulysses ranks (one TMA
+// tensor map per shard: the pre-attention exchange fused into the loads).
 //
 // TMEM (512 columns x 128 lanes, fp32):
 //   [  0,128) S buffer 0    [128,256) S buffer 1        (scores, double-buffered)
@@ -64,9 +74,9 @@ namespace {
 
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_N = 128;
-constexpr int NUM_THREADS = 352;
+constexpr int NUM_THREADS = 384;
 constexpr int NUM_SOFTMAX_WARPS = 8;
-constexpr int WARP_TMA = 8;
+constexpr int WARP_TMA = 11;
 constexpr int WARP_MMA_S = 9;
 constexpr int WARP_MMA_PV = 10;
 constexpr uint32_t TMEM_COLS = 512;
@@ -801,7 +811,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorM
             producer_role<D>(tq, tk, tv, args, smem, bar0, abort_flag);
         else if (warp == WARP_MMA_S)
             mma_s_role<D>(args, smem, bar0, tmem_base, abort_flag);
-        else
+        else if (warp == WARP_MMA_PV)
             mma_pv_role<D>(args, smem, bar0, tmem_base, abort_flag);
     }
     __syncwarp();
