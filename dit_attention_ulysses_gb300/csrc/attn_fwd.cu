@@ -343,15 +343,17 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
 }
 
 // --------------------------------------------------------------------- MMA
-// Q / K operand (K-major, 128-B swizzle): k-step kk covers 16 columns of D.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
-    return smem_desc_sw128(tile_addr + (kk >> 2) * PANEL_BYTES + (kk & 3) * 32, 16, 1024);
+// Shared-memory operand descriptors (128-byte swizzle) are built once per role;
+// a k-step or a ring stage only moves the start address (desc_add, one 32-bit
+// add), which keeps the issuing threads to a few instructions per MMA.
+// Q / K operand (K-major): k-step kk covers 16 columns of D, 32 B within the
+// 128-B rows of a 64-column panel; panels are PANEL_BYTES apart.
+__device__ __forceinline__ constexpr uint32_t k_step16(int kk) {
+    return static_cast<uint32_t>((kk >> 2) * (PANEL_BYTES >> 4) + (kk & 3) * 2);
 }
-// V operand (MN-major = D contiguous, 128-B swizzle): k-step kk covers 16 keys;
-// 8-key groups are 1024 B apart (SBO), 64-wide D panels PANEL_BYTES apart (LBO).
-__device__ __forceinline__ uint64_t vmajor_desc(uint32_t tile_addr, int kk) {
-    return smem_desc_sw128(tile_addr + kk * 2048, PANEL_BYTES, 1024);
-}
+// V operand (MN-major = D contiguous): k-step kk covers 16 keys = two 8-key
+// groups of 1024 B (SBO); 64-wide D panels are PANEL_BYTES apart (LBO).
+__device__ __forceinline__ constexpr uint32_t v_step16(int kk) { return static_cast<uint32_t>(kk * (2048 >> 4)); }
 
 // Issuer of S(j) = Q K_j^T (SS) into S buffer (block index) & 1.  One thread.
 template <int D>
@@ -361,6 +363,8 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
     constexpr uint32_t IDESC_QK = idesc_bf16_f32(BLOCK_M, BLOCK_N, 0);
+    const uint64_t qdesc0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);   // Q buffer 0
+    const uint64_t kdesc0 = smem_desc_sw128(sbase + C::KV_OFF, 16, 1024);  // ring stage 0, as K
     uint32_t g = 0;      // key blocks over the CTA's lifetime
     uint32_t item0 = 0;  // first ring item of the current piece of work
     int u_iter = 0;
@@ -369,7 +373,7 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
     for (; ok && get_work(a, u_iter, w); ++u_iter) {
         const int n = w.nb;
         const int qb = u_iter % C::Q_BUFS;
-        const uint32_t qaddr = sbase + C::Q_OFF + qb * C::TILE_BYTES;
+        const uint64_t qdesc = desc_add(qdesc0, qb * (C::TILE_BYTES >> 4));
         ok = thread_wait(bar(C::B_Q_FULL + qb), (u_iter / C::Q_BUFS) & 1, abort_flag, a.timeout_ns);
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gs = g + j;
@@ -381,10 +385,11 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
             if (ok) ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t kaddr = sbase + C::KV_OFF + stage * C::TILE_BYTES;
+            const uint64_t kdesc = desc_add(kdesc0, stage * (C::TILE_BYTES >> 4));
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(tmem_base + S_COL + sb * 128u, kmajor_desc(qaddr, kk), kmajor_desc(kaddr, kk), IDESC_QK, kk > 0);
+                mma_ss(tmem_base + S_COL + sb * 128u, desc_add(qdesc, k_step16(kk)), desc_add(kdesc, k_step16(kk)),
+                       IDESC_QK, kk > 0);
             mma_commit(bar(C::B_S_FULL + sb));
             mma_commit(bar(C::B_KV_FREE + stage));
             if (j == n - 1) mma_commit(bar(C::B_Q_FREE + qb));
@@ -407,6 +412,7 @@ __device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uin
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
     constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 1);
+    const uint64_t vdesc0 = smem_desc_sw128(sbase + C::KV_OFF, PANEL_BYTES, 1024);  // ring stage 0, as V
     uint32_t g = 0;
     uint32_t item0 = 0;
     int u_iter = 0;
@@ -425,11 +431,11 @@ __device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uin
             if (ok) ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t vaddr = sbase + C::KV_OFF + stage * C::TILE_BYTES;
+            const uint64_t vdesc = desc_add(vdesc0, stage * (C::TILE_BYTES >> 4));
 #pragma unroll
             for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-                mma_ts(tmem_base + O_COL, tmem_base + P_COL + pb * 64u + kk * 8, vmajor_desc(vaddr, kk), IDESC_PV,
-                       (j > 0) || (kk > 0));
+                mma_ts(tmem_base + O_COL, tmem_base + P_COL + pb * 64u + kk * 8, desc_add(vdesc, v_step16(kk)),
+                       IDESC_PV, (j > 0) || (kk > 0));
             mma_commit(bar(C::B_P_FREE + pb));
             mma_commit(bar(C::B_KV_FREE + stage));
             if (j == n - 1) mma_commit(bar(C::B_O_FINAL));

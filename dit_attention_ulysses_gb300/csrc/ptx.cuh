@@ -225,6 +225,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// A descriptor moved by `off16` x 16 bytes.  The start-address field (bits
+// 0-13, address >> 4) of any shared-memory address below 256 KB plus such an
+// offset stays below 2^14, so a 32-bit add on the low word cannot carry out of
+// the field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
+    const uint32_t lo = static_cast<uint32_t>(d) + off16;
+    return (static_cast<uint64_t>(static_cast<uint32_t>(d >> 32)) << 32) | lo;
+}
+
 // Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, dense.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //   bit 15 A major (0 = K), bit 16 B major (0 = K, 1 = MN),
