@@ -27,6 +27,7 @@ __all__ = [
     "xs_relayout_a2a",
     "xs_relayout_a2a_inverse",
     "xs_attn_ulysses_fwd",
+    "xs_burst_gap",
     "xs_attn_a2a_fwd_staged",
     "xs_attn_workspace_bytes",
     "xs_attn_fwd_balanced",
@@ -83,6 +84,7 @@ EXPORTS = {
                                    ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32, _vp, _size, _vp]),
     "xs_relayout_a2a_inverse": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int, _int, _int, _int,
                                        _vp]),
+    "xs_burst_gap": (_int, [_vp, _size, _int, _size, _int, ctypes.c_longlong, ctypes.c_longlong, _vp, _vp]),
     "xs_attn_get_device_error": (_int, [_vp]),
     "xs_attn_error_string": (ctypes.c_char_p, [_int]),
     "xs_attn_last_cuda_error": (_int, []),
@@ -201,6 +203,18 @@ def xs_relayout_a2a_inverse(seq_shards, heads, stream=None) -> None:
     B, Sl, H, D = ss[0].shape
     _check(lib.xs_relayout_a2a_inverse(_ptr_array([x.data_ptr() for x in ss]), _ptr_array([x.data_ptr() for x in hs]),
                                        B, Sl * P, H, D, P, _stream_handle(stream)), "xs_relayout_a2a_inverse")
+
+
+def xs_burst_gap(dst, producers: int, burst_bytes: int, bursts: int, gap_ns: int, stream=None, lead_ns: int = 0):
+    """Run the Burst-Gap store microbenchmark into the CUDA tensor ``dst`` (any dtype, contiguous);
+    returns the device int64 tensor [bursts, producers] of burst issue times in ns."""
+    import torch
+    if not dst.is_cuda or not dst.is_contiguous():
+        raise TypeError("dst must be a contiguous CUDA tensor")
+    times = torch.empty((bursts, producers), dtype=torch.int64, device=dst.device)
+    _check(lib.xs_burst_gap(dst.data_ptr(), dst.numel() * dst.element_size(), producers, burst_bytes, bursts,
+                            lead_ns, gap_ns, times.data_ptr(), _stream_handle(stream)), "xs_burst_gap")
+    return times
 
 
 def xs_attn_a2a_fwd_staged(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, scale: float,

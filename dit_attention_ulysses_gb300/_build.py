@@ -14,7 +14,7 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libxsattn.so")
-SOURCES = ["attn_fwd.cu", "relayout.cu", "api.cu"]
+SOURCES = ["attn_fwd.cu", "relayout.cu", "burst_gap.cu", "api.cu"]
 HEADERS = ["kernels.h", "ptx.cuh", os.path.join("..", "..", "include", "xsattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -603,6 +603,38 @@ int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v
     return XS_OK;
 }
 
+int xs_burst_gap(void* dst, size_t dst_bytes, int producers, size_t burst_bytes, int bursts, long long lead_ns,
+                 long long gap_ns, long long* issue_ns, void* stream) {
+    if (!dst || !issue_ns) return XS_ERR_NULL;
+    if (producers < 1 || bursts < 1 || bursts > 65536 || gap_ns < 0 || gap_ns > 100000000LL) return XS_ERR_SHAPE;
+    if (lead_ns < 0 || lead_ns > 100000000LL) return XS_ERR_SHAPE;
+    if (static_cast<double>(bursts) * static_cast<double>(gap_ns) > 1e10) return XS_ERR_SHAPE;  // <= 10 s of gaps
+    const size_t per = burst_bytes / static_cast<size_t>(producers);
+    if (burst_bytes == 0 || burst_bytes % (16u * static_cast<size_t>(producers)) != 0) return XS_ERR_SHAPE;
+    const size_t windows = dst_bytes / per;
+    if (windows < static_cast<size_t>(producers)) return XS_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) != 0 || (reinterpret_cast<uintptr_t>(issue_ns) & 7u) != 0)
+        return XS_ERR_ALIGNMENT;
+    const int64_t times_bytes = static_cast<int64_t>(bursts) * producers * 8;
+    if (overlaps(range_of(dst, static_cast<int64_t>(dst_bytes)), range_of(issue_ns, times_bytes)))
+        return XS_ERR_OVERLAP;
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc != XS_OK) return rc;
+    if (producers > dev.sms) return XS_ERR_SHAPE;
+    xs::BurstGapArgs a;
+    a.dst = dst;
+    a.chunks_per_producer = static_cast<int64_t>(per / 16);
+    a.windows = static_cast<int64_t>(windows);
+    a.bursts = bursts;
+    a.lead_ns = lead_ns;
+    a.gap_ns = gap_ns;
+    a.issue_ns = issue_ns;
+    cudaError_t e = xs::launch_burst_gap(a, producers, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return XS_OK;
+}
+
 int xs_attn_get_device_error(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);

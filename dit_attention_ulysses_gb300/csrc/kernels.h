@@ -94,4 +94,17 @@ cudaError_t launch_relayout(const RelayoutArgs& a, int num_sms, cudaStream_t str
 // [B, S, H/P, D].
 cudaError_t launch_relayout_inverse(const RelayoutArgs& a, int num_sms, cudaStream_t stream);
 
+// Burst-Gap microbenchmark of the store path (csrc/burst_gap.cu).
+struct BurstGapArgs {
+    void* dst;                   // destination buffer, 16-byte aligned
+    int64_t chunks_per_producer; // 16-byte chunks each producer stores per burst (V / K / 16)
+    int64_t windows;             // dst holds this many producer windows (rotated through)
+    int bursts;
+    long long lead_ns;           // spin before the first burst
+    long long gap_ns;            // producer-side gap after each burst
+    long long* issue_ns;         // device [bursts][producers]: issue time of each burst
+};
+
+cudaError_t launch_burst_gap(const BurstGapArgs& a, int producers, cudaStream_t stream);
+
 }  // namespace xs

@@ -259,6 +259,37 @@ int xs_attn_fwd_balanced_noalloc(const void* q, const void* k, const void* v, in
                                  int B, int S, int H, int D, int P, float scale, void* stream);
 
 /*
+ * xs_burst_gap -- Burst-Gap microbenchmark of the store path the fused epilogue
+ * uses (SM -> L2 -> HBM on one GPU).  X-Stage (arXiv 2607.23264), gist.science
+ * technical summary, "Methodology: The X-Stage Abstraction and Burst-Gap
+ * Model": K producers issue bursts of stores of aggregate volume V separated
+ * by a producer-side gap G; the sender-visible issue time of a burst is
+ *     T_iss(G; K, V) = max(T0_iss(K, V), V / R - G),
+ * with T0_iss the backpressure-free issue time, R the effective drain rate and
+ * Q the outstanding capacity of the path.  This kernel produces the raw issue
+ * times; the fit is dit_attention_ulysses_gb300/burst_gap.py.
+ *   dst         device buffer the bursts are stored to (16-byte aligned),
+ *               dst_bytes long; producer windows of burst_bytes/producers bytes
+ *               rotate through it (use one larger than L2 to reach HBM).
+ *               Contents afterwards: the 16-byte pattern
+ *               {i, r, c, i ^ 0x9E3779B9} at chunk i of the window of burst r,
+ *               producer c (later bursts overwrite earlier ones).
+ *   producers   K, 1 <= K <= the SM count (one CTA per SM).
+ *   burst_bytes V, a multiple of 16 * producers; dst_bytes / (V/K) >= K.
+ *   bursts      1 <= bursts <= 65536;  gap_ns  0 <= G <= 1e8, bursts * G <= 1e10.
+ *   lead_ns     0 <= lead_ns <= 1e8: a spin before the first burst (the path
+ *               drains from earlier work while the SMs stay busy).
+ *   issue_ns    device int64 array [bursts][producers] (8-byte aligned, not
+ *               inside dst): the issue time of burst r at producer c, from
+ *               before its first store to after its last thread issued its
+ *               last store (%globaltimer, ns).
+ * Returns XS_OK or XS_ERR_NULL / _SHAPE / _ALIGNMENT / _OVERLAP /
+ * _UNSUPPORTED_DEVICE / _CUDA; asynchronous on `stream`.
+ */
+int xs_burst_gap(void* dst, size_t dst_bytes, int producers, size_t burst_bytes, int bursts,
+                 long long lead_ns, long long gap_ns, long long* issue_ns, void* stream);
+
+/*
  * xs_attn_get_device_error -- synchronises `stream`, then reads and clears the
  * library's device error word on the current device.  Returns XS_OK, or
  * XS_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel expired (the kernel
