@@ -97,7 +97,9 @@ struct Cfg {
     static constexpr int XCH_OFF = KV_OFF + KV_STAGES * TILE_BYTES;  // row max / row sum exchange
     static constexpr int XMAX_BYTES = 2 * 2 * BLOCK_M * 4;           // [block parity][half][row] fp32
     static constexpr int XCH_BYTES = XMAX_BYTES + 2 * BLOCK_M * 4;   // + sums [half][row]
-    static constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
+    static constexpr int STAGE_OFF = XCH_OFF + XCH_BYTES;            // epilogue staging, 2 KB per softmax warp
+    static constexpr int STAGE_BYTES = NUM_SOFTMAX_WARPS * 2048;
+    static constexpr int BAR_OFF = STAGE_OFF + STAGE_BYTES;
     // barrier indices
     static constexpr int B_Q_FULL = 0;                 // [2]  TMA -> MMA, per Q buffer
     static constexpr int B_Q_FREE = 2;                 // [2]  MMA -> TMA
@@ -726,16 +728,22 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
         if (!ok) break;
         tc_fence_after();
         if (w.kind == WORK_FULL) {
+            // Each lane holds one row; stores straight from the lanes would scatter
+            // 32 rows per instruction.  A 2 KB per-warp stage (32 rows x 64 B,
+            // 16-byte chunks XOR-swizzled against bank conflicts) lets 4 lanes write
+            // 64 contiguous bytes of a row: each store instruction covers 8 rows.
             const int s_row = qt * BLOCK_M + row;
-            const bool store = s_row < a.S;
-            __nv_bfloat16* dst = nullptr;
-            if (store) {
+            unsigned long long dst_row = 0;   // this lane's row in the destination (0: past S)
+            if (s_row < a.S) {
                 const int p = s_row / a.epi.Sl + h / a.epi.Hl;
                 const int s_dst = s_row % a.epi.Sl;
                 const int h_dst = h % a.epi.Hl;
-                dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
-                      ((static_cast<size_t>(b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D + half * DH;
+                dst_row = reinterpret_cast<unsigned long long>(
+                    reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
+                    ((static_cast<size_t>(b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D + half * DH);
             }
+            uint4* stage = reinterpret_cast<uint4*>(smem + C::STAGE_OFF + warp * 2048);
+            const int lane = static_cast<int>(lane_id());
             const float inv_l = 1.0f / l_row;
 #pragma unroll
             for (int q = 0; q < DH / 32; ++q) {
@@ -746,11 +754,21 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     wv[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
-                if (store) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        st_global_v4(dst + q * 32 + v4 * 8, wv[4 * v4], wv[4 * v4 + 1], wv[4 * v4 + 2], wv[4 * v4 + 3]);
+                for (int c4 = 0; c4 < 4; ++c4)
+                    stage[lane * 4 + (c4 ^ (lane & 3))] =
+                        make_uint4(wv[4 * c4], wv[4 * c4 + 1], wv[4 * c4 + 2], wv[4 * c4 + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = k * 8 + (lane >> 2);   // row (lane of the warp) this lane stores a chunk of
+                    const int c4 = lane & 3;
+                    const uint4 v = stage[r * 4 + (c4 ^ (r & 3))];
+                    const unsigned long long rp = __shfl_sync(0xffffffffu, dst_row, r);
+                    if (rp)
+                        st_global_v4(reinterpret_cast<__nv_bfloat16*>(rp) + q * 32 + c4 * 8, v.x, v.y, v.z, v.w);
                 }
+                __syncwarp();   // the stage is rewritten by the next chunk
             }
         } else {
             ok = split_epilogue<D>(a, w, t_base + O_COL + half * DH, row, half, warp, m_run, l_row, abort_flag);
