@@ -237,3 +237,24 @@ def test_balanced_expired_wait_is_reported(xs, monkeypatch):
     ref = oracle.attention_a2a(qb, kb, vb, w.scale, P)
     mass = oracle.attention_a2a(qb, kb, abs_bits(vb), w.scale, P)
     assert_close(np.stack([torch_to_f64(o) for o in outs]), ref, mass, "balanced after timeout")
+
+
+def test_staged_host_entry_with_workspace_matches_device_entry(xs):
+    """xs_attn_a2a_fwd_staged with a workspace (H2D, balanced kernel, D2H on one
+    stream) returns exactly the shards of the device-side balanced call."""
+    S, D, P, B, H = SHAPES[0]
+    _check_splits(B, S, H)
+    ws = xs.Workspace(xs.xs_attn_workspace_bytes(B, S, H, D))
+    w = di.Workload("st", B=B, H=H, S=S, D=D, P=P, scale=1 / math.sqrt(D), seed=17)
+    bits = di.random_qkv(w)
+    qd, kd, vd = (bits_to_torch(x) for x in bits)
+    ref = _run(xs, qd, kd, vd, w.scale, P, ws)
+    pin = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).pin_memory()
+    qh, kh, vh = (pin(x) for x in bits)
+    out_h = [torch.empty((B, S // P, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(P)]
+    out_d = _shards(B, S, H, D, P)
+    xs.xs_attn_a2a_fwd_staged(qh, kh, vh, out_h, qd, kd, vd, out_d, w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert xs.xs_attn_get_device_error() == xs.XS_OK
+    for a, b in zip(out_h, ref):
+        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
