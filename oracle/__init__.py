@@ -12,6 +12,8 @@ attention) and the gist.science technical summary, "Key Contributions" item 3
 (FlashAttention-A2A piggybacking).  The pages do not spell out attention
 itself; the oracle takes the textbook definition O = softmax(Q K^T * scale) V,
 non-causal, no mask, no bias, fp64 throughout (see ``attention_oracle.c``).
+``causal=True`` selects the causal variant, which the pages do not treat: row i
+attends to keys 0 .. i only (plain attention over the first i + 1 keys).
 
 Every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py`` (brute force, closed forms, invariants, an exact
@@ -53,16 +55,18 @@ def _load():
         if _lib is None:
             build()
             lib = ctypes.CDLL(_LIB)
-            lib.oracle_attention.restype = ctypes.c_int
-            lib.oracle_attention.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64,
-                                             ctypes.c_double, _ptr, ctypes.c_int]
-            lib.oracle_attention_rows.restype = ctypes.c_int
-            lib.oracle_attention_rows.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64,
-                                                  ctypes.c_double, _ptr, _ptr, _i64, _ptr,
-                                                  ctypes.c_int]
-            lib.oracle_attention_weights.restype = ctypes.c_int
-            lib.oracle_attention_weights.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64,
-                                                     ctypes.c_double, _i64, _i64, _i64, _ptr, _ptr]
+            for suffix in ("", "_causal"):
+                f = getattr(lib, "oracle_attention" + suffix)
+                f.restype = ctypes.c_int
+                f.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, ctypes.c_double, _ptr, ctypes.c_int]
+                f = getattr(lib, "oracle_attention_rows" + suffix)
+                f.restype = ctypes.c_int
+                f.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, ctypes.c_double, _ptr, _ptr, _i64, _ptr,
+                              ctypes.c_int]
+                f = getattr(lib, "oracle_attention_weights" + suffix)
+                f.restype = ctypes.c_int
+                f.argtypes = [_ptr, _ptr, _ptr, _i64, _i64, _i64, _i64, ctypes.c_double, _i64, _i64, _i64, _ptr,
+                              _ptr]
             for name in ("oracle_head_shards", "oracle_a2a", "oracle_a2a_inverse"):
                 f = getattr(lib, name)
                 f.restype = ctypes.c_int
@@ -93,42 +97,48 @@ def threads_used(nthreads: int | None = None) -> int:
     return _load().oracle_max_threads(nthreads or default_threads())
 
 
-def attention(q, k, v, scale: float, nthreads: int | None = None) -> np.ndarray:
+def _fn(name: str, causal: bool):
+    return getattr(_load(), name + ("_causal" if causal else ""))
+
+
+def attention(q, k, v, scale: float, nthreads: int | None = None, causal: bool = False) -> np.ndarray:
     """Exact attention O [B,S,H,D] (float64) of bf16-bit inputs [B,S,H,D]."""
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, S, H, D = q.shape
     assert k.shape == q.shape and v.shape == q.shape
     o = np.empty((B, S, H, D), dtype=np.float64)
-    rc = _load().oracle_attention(_p(q), _p(k), _p(v), B, S, H, D, float(scale), _p(o),
-                                  nthreads or default_threads())
+    rc = _fn("oracle_attention", causal)(_p(q), _p(k), _p(v), B, S, H, D, float(scale), _p(o),
+                                         nthreads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_attention failed ({rc})")
     return o
 
 
-def attention_rows(q, k, v, scale: float, rows_b, rows_s, nthreads: int | None = None) -> np.ndarray:
+def attention_rows(q, k, v, scale: float, rows_b, rows_s, nthreads: int | None = None,
+                   causal: bool = False) -> np.ndarray:
     """Exact attention of selected query rows: returns [n_rows, H, D] float64."""
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, S, H, D = q.shape
     rb = np.ascontiguousarray(rows_b, dtype=np.int64)
     rs = np.ascontiguousarray(rows_s, dtype=np.int64)
     o = np.empty((len(rb), H, D), dtype=np.float64)
-    rc = _load().oracle_attention_rows(_p(q), _p(k), _p(v), B, S, H, D, float(scale),
-                                       _p(rb), _p(rs), len(rb), _p(o),
-                                       nthreads or default_threads())
+    rc = _fn("oracle_attention_rows", causal)(_p(q), _p(k), _p(v), B, S, H, D, float(scale),
+                                              _p(rb), _p(rs), len(rb), _p(o),
+                                              nthreads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_attention_rows failed ({rc})")
     return o
 
 
-def attention_weights(q, k, v, scale: float, b: int, i: int, h: int):
-    """Normalised softmax weights w[S] and output row o[D] of query (b, i, h)."""
+def attention_weights(q, k, v, scale: float, b: int, i: int, h: int, causal: bool = False):
+    """Normalised softmax weights w[S] and output row o[D] of query (b, i, h)
+    (causal: w[j] = 0 for j > i)."""
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, S, H, D = q.shape
     w = np.empty(S, dtype=np.float64)
     o = np.empty(D, dtype=np.float64)
-    rc = _load().oracle_attention_weights(_p(q), _p(k), _p(v), B, S, H, D, float(scale),
-                                          b, i, h, _p(w), _p(o))
+    rc = _fn("oracle_attention_weights", causal)(_p(q), _p(k), _p(v), B, S, H, D, float(scale),
+                                                 b, i, h, _p(w), _p(o))
     if rc != 0:
         raise RuntimeError("oracle_attention_weights failed")
     return w, o
@@ -164,12 +174,12 @@ def a2a_inverse(out: np.ndarray) -> np.ndarray:
     return L
 
 
-def attention_a2a(q, k, v, scale: float, P: int, nthreads: int | None = None) -> np.ndarray:
+def attention_a2a(q, k, v, scale: float, P: int, nthreads: int | None = None, causal: bool = False) -> np.ndarray:
     """The whole oracle path: attention, then the explicit Ulysses re-shard.
 
     Returns the P output shards as one array [P, B, S/P, H, D] (float64).
     """
-    return a2a(head_shards(attention(q, k, v, scale, nthreads), P))
+    return a2a(head_shards(attention(q, k, v, scale, nthreads, causal), P))
 
 
 def _exact_bf16_bits(x: np.ndarray) -> np.ndarray:

@@ -27,6 +27,13 @@
  *      the rows of p's contiguous sequence block:
  *        out_p[b,s',r*H/P + j,d] = L_r[b, p*S/P + s', j, d],   s' < S/P.
  *
+ *   3. Causal variant (not on the pages, which treat bidirectional DiT
+ *      attention; it is the masked self-attention of autoregressive models):
+ *      query row i attends to keys j <= i only, i.e. definition 1 with every
+ *      sum and the max running over j = 0 .. i.  Row i of the causal result is
+ *      therefore row i of plain attention over the first i + 1 keys and values,
+ *      which is how it is computed below (the same row routine, n_keys = i + 1).
+ *
  * Inputs are bf16 bit patterns (uint16) in [B,S,H,D] layout, D fastest; they
  * are widened to double exactly.  Outputs are double.
  */
@@ -58,7 +65,7 @@ static void widen_head(const uint16_t* t, double* dst, int64_t b, int64_t h,
 }
 
 /*
- * One query row of exact softmax attention.
+ * One query row of exact softmax attention over keys 0 .. S-1.
  *   qrow [D], kd/vd [S][D] (double), x: scratch [S] (receives the normalised
  *   weights w_j / l on return), orow [D] output.
  */
@@ -102,17 +109,13 @@ static int set_threads(int nthreads) {
 /* Number of threads the OpenMP runtime will use for the next parallel region. */
 int oracle_max_threads(int nthreads) { return set_threads(nthreads); }
 
-/*
- * Selected query rows of exact attention.
- *   q, k, v : bf16 bits [B,S,H,D]
- *   rows_b, rows_s : n_rows query positions (b, s)
- *   o_rows  : double [n_rows, H, D] output (row r, head h at (r*H + h)*D)
- * Returns 0, or -1 on allocation failure / bad arguments.
- */
-int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                          int64_t B, int64_t S, int64_t H, int64_t D, double scale,
-                          const int64_t* rows_b, const int64_t* rows_s, int64_t n_rows,
-                          double* o_rows, int nthreads) {
+/* Keys that query row i attends to: all S, or (causal) keys 0 .. i. */
+static int64_t keys_of_row(int64_t i, int64_t S, int causal) { return causal ? i + 1 : S; }
+
+static int attention_rows_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                               const int64_t* rows_b, const int64_t* rows_s, int64_t n_rows,
+                               double* o_rows, int nthreads, int causal) {
     if (B < 1 || S < 1 || H < 1 || D < 1 || n_rows < 0) return -1;
     for (int64_t r = 0; r < n_rows; ++r)
         if (rows_b[r] < 0 || rows_b[r] >= B || rows_s[r] < 0 || rows_s[r] >= S) return -1;
@@ -142,7 +145,8 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
                         if (rows_b[r] != b) continue;
                         for (int64_t d = 0; d < D; ++d)
                             qrow[d] = bf16_to_double(q[idx4(b, rows_s[r], h, d, S, H, D)]);
-                        attention_row(qrow, kd, vd, S, D, scale, x, o_rows + (size_t)((r * H + h) * D));
+                        attention_row(qrow, kd, vd, keys_of_row(rows_s[r], S, causal), D, scale, x,
+                                      o_rows + (size_t)((r * H + h) * D));
                     }
                 }
                 free(x);
@@ -156,11 +160,30 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
 }
 
 /*
- * Full exact attention: o is double [B,S,H,D].
+ * Selected query rows of exact attention.
+ *   q, k, v : bf16 bits [B,S,H,D]
+ *   rows_b, rows_s : n_rows query positions (b, s)
+ *   o_rows  : double [n_rows, H, D] output (row r, head h at (r*H + h)*D)
+ * Returns 0, or -1 on allocation failure / bad arguments.
  */
-int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                     int64_t B, int64_t S, int64_t H, int64_t D, double scale,
-                     double* o, int nthreads) {
+int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                          const int64_t* rows_b, const int64_t* rows_s, int64_t n_rows,
+                          double* o_rows, int nthreads) {
+    return attention_rows_impl(q, k, v, B, S, H, D, scale, rows_b, rows_s, n_rows, o_rows, nthreads, 0);
+}
+
+/* The same rows of causal attention (row s attends to keys 0 .. s). */
+int oracle_attention_rows_causal(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                                 const int64_t* rows_b, const int64_t* rows_s, int64_t n_rows,
+                                 double* o_rows, int nthreads) {
+    return attention_rows_impl(q, k, v, B, S, H, D, scale, rows_b, rows_s, n_rows, o_rows, nthreads, 1);
+}
+
+static int attention_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                          double* o, int nthreads, int causal) {
     if (B < 1 || S < 1 || H < 1 || D < 1) return -1;
     set_threads(nthreads);
     double* kd = (double*)malloc(sizeof(double) * (size_t)(S * D));
@@ -183,7 +206,7 @@ int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 #pragma omp for schedule(static)
                     for (int64_t i = 0; i < S; ++i) {
                         for (int64_t d = 0; d < D; ++d) qrow[d] = bf16_to_double(q[idx4(b, i, h, d, S, H, D)]);
-                        attention_row(qrow, kd, vd, S, D, scale, x, orow);
+                        attention_row(qrow, kd, vd, keys_of_row(i, S, causal), D, scale, x, orow);
                         for (int64_t d = 0; d < D; ++d) o[idx4(b, i, h, d, S, H, D)] = orow[d];
                     }
                 }
@@ -199,12 +222,24 @@ int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 }
 
 /*
- * The normalised softmax weights of one query row (b, i, h): w[S], sum 1.
- * Exposed so that the row-sum and non-negativity of the weights can be checked.
+ * Full exact attention: o is double [B,S,H,D].
  */
-int oracle_attention_weights(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                             int64_t B, int64_t S, int64_t H, int64_t D, double scale,
-                             int64_t b, int64_t i, int64_t h, double* w, double* orow) {
+int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                     double* o, int nthreads) {
+    return attention_impl(q, k, v, B, S, H, D, scale, o, nthreads, 0);
+}
+
+/* Full exact causal attention: o is double [B,S,H,D]. */
+int oracle_attention_causal(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                            double* o, int nthreads) {
+    return attention_impl(q, k, v, B, S, H, D, scale, o, nthreads, 1);
+}
+
+static int attention_weights_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                                  int64_t b, int64_t i, int64_t h, double* w, double* orow, int causal) {
     if (b < 0 || b >= B || i < 0 || i >= S || h < 0 || h >= H) return -1;
     double* kd = (double*)malloc(sizeof(double) * (size_t)(S * D));
     double* vd = (double*)malloc(sizeof(double) * (size_t)(S * D));
@@ -213,11 +248,30 @@ int oracle_attention_weights(const uint16_t* q, const uint16_t* k, const uint16_
     widen_head(k, kd, b, h, S, H, D);
     widen_head(v, vd, b, h, S, H, D);
     for (int64_t d = 0; d < D; ++d) qrow[d] = bf16_to_double(q[idx4(b, i, h, d, S, H, D)]);
-    attention_row(qrow, kd, vd, S, D, scale, w, orow);
+    const int64_t n = keys_of_row(i, S, causal);
+    attention_row(qrow, kd, vd, n, D, scale, w, orow);
+    for (int64_t j = n; j < S; ++j) w[j] = 0.0;   /* keys the row does not attend to */
     free(kd);
     free(vd);
     free(qrow);
     return 0;
+}
+
+/*
+ * The normalised softmax weights of one query row (b, i, h): w[S], sum 1.
+ * Exposed so that the row-sum and non-negativity of the weights can be checked.
+ */
+int oracle_attention_weights(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                             int64_t b, int64_t i, int64_t h, double* w, double* orow) {
+    return attention_weights_impl(q, k, v, B, S, H, D, scale, b, i, h, w, orow, 0);
+}
+
+/* The same for causal attention: w[j] = 0 for j > i, sum over j <= i is 1. */
+int oracle_attention_weights_causal(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                                    int64_t b, int64_t i, int64_t h, double* w, double* orow) {
+    return attention_weights_impl(q, k, v, B, S, H, D, scale, b, i, h, w, orow, 1);
 }
 
 /*
