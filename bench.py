@@ -286,6 +286,12 @@ def run_ours(args, rank, world, local_rank):
                 xs.xs_attn_fwd(pre[0][r], pre[1][r], pre[2][r], o_heads[r], w.scale, stream)
             xs.xs_relayout_a2a(o_heads, uly_serial, stream)
 
+    # causal variant (row s attends to keys 0 .. s) with the same fused A2A stores
+    causal_out = [torch.empty(shard_shape, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+
+    def causal():
+        xs.xs_attn_causal_fwd(q, k, v, xs.XS_LAYOUT_A2A, causal_out, w.scale, stream)
+
     for _ in range(max(3, args.warmup)):
         fused()
     torch.cuda.synchronize()
@@ -316,18 +322,25 @@ def run_ours(args, rank, world, local_rank):
     # ablation: attention alone (contiguous store), fused, and attention + separate
     # re-layout, interleaved run by run so that clock drift affects all three alike
     n_abl = max(10, min(args.steps, 50))
-    for fn in (alone, serial_path) + ((ulysses_fused, ulysses_serial) if uly else ()):
+    for fn in (alone, serial_path, causal) + ((ulysses_fused, ulysses_serial) if uly else ()):
         for _ in range(3):
             fn()
-    ta, tf, ts, tuf, tus = [], [], [], [], []
+    ta, tf, ts, tc, tuf, tus = [], [], [], [], [], []
     for _ in range(n_abl):
         ta += time_steps(torch, alone, 1, flush, stream)
         tf += time_steps(torch, fused, 1, flush, stream)
         ts += time_steps(torch, serial_path, 1, flush, stream)
+        tc += time_steps(torch, causal, 1, flush, stream)
         if uly:
             tuf += time_steps(torch, ulysses_fused, 1, flush, stream)
             tus += time_steps(torch, ulysses_serial, 1, flush, stream)
     t_alone, t_fused, t_serial = statistics.median(ta), statistics.median(tf), statistics.median(ts)
+    # causal tensor FLOPs: 4*D per unmasked (query, key) pair, S*(S+1)/2 pairs per (b, h)
+    causal_flops = 2 * B * H * D * S * (S + 1)
+    t_causal = statistics.median(tc)
+    causal_line = {"api": "xs_attn_causal_fwd", "ms": t_causal, "tflops": causal_flops / (t_causal * 1e-3) / 1e12,
+                   "flops": causal_flops, "flops_rule": "4*B*H*D*S*(S+1)/2 (unmasked query-key pairs)",
+                   "over_bidirectional_fused_ms": t_causal / t_fused, "runs": n_abl, "statistic": "median"}
     ulysses = None
     if uly:
         t_uf, t_us = statistics.median(tuf), statistics.median(tus)
@@ -384,6 +397,7 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": 3 * w.tensor_bytes, "d2h_bytes_per_step": w.tensor_bytes,
                 "ms_per_step": e2e_ms, "api": "xs_attn_a2a_fwd_staged"},
         "ulysses_step": ulysses,
+        "causal": causal_line,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),

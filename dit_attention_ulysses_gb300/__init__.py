@@ -32,6 +32,7 @@ __all__ = [
     "xs_attn_workspace_bytes",
     "xs_attn_fwd_balanced",
     "xs_attn_fwd_balanced_noalloc",
+    "xs_attn_causal_fwd",
     "Workspace",
     "xs_attn_get_device_error",
     "xs_attn_error_string",
@@ -80,6 +81,8 @@ EXPORTS = {
                                     _vp, _size, _vp]),
     "xs_attn_fwd_balanced_noalloc": (_int, [_vp, _vp, _vp, _int, ctypes.POINTER(_vp), _int, _int, _int, _int, _int,
                                             _f32, _vp]),
+    "xs_attn_causal_fwd": (_int, [_vp, _vp, _vp, _int, ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32,
+                                  _vp]),
     "xs_attn_ulysses_fwd": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                    ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32, _vp, _size, _vp]),
     "xs_relayout_a2a_inverse": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int, _int, _int, _int,
@@ -292,6 +295,18 @@ def xs_attn_fwd_balanced_noalloc(q, k, v, layout: int, outs, scale: float, strea
     _check(lib.xs_attn_fwd_balanced_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), layout,
                                             _ptr_array([o.data_ptr() for o in os_]), B, S, H, D, len(os_), scale,
                                             _stream_handle(stream)), "xs_attn_fwd_balanced_noalloc")
+
+
+def xs_attn_causal_fwd(q, k, v, layout: int, outs, scale: float, stream=None) -> None:
+    """Causal attention (row s attends to keys 0 .. s) with the fused output layouts:
+    ``layout`` XS_LAYOUT_A2A (P sequence shards), XS_LAYOUT_CONTIGUOUS (one [B,S,H,D]
+    tensor) or XS_LAYOUT_HEADS (P head shards)."""
+    B, S, H, D = _bshd(q, "q").shape
+    _bshd(k, "k"), _bshd(v, "v")
+    os_ = [_bshd(o, "out") for o in outs]
+    _check(lib.xs_attn_causal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), layout,
+                                  _ptr_array([o.data_ptr() for o in os_]), B, S, H, D, len(os_), scale,
+                                  _stream_handle(stream)), "xs_attn_causal_fwd")
 
 
 def attn_a2a(q, k, v, P: int, scale: float | None = None, stream=None, workspace=None):

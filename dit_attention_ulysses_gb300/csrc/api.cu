@@ -247,14 +247,16 @@ unsigned next_epoch() {
 // Inputs: q, k, v each one [B,S,H,D] tensor, or (shards != nullptr) the P
 // sequence shards [B,S/P,H,D] of each operand: shards[0..P) = q, [P..2P) = k,
 // [2P..3P) = v, with (S/P) % 128 == 0.
+// causal: row s attends to keys 0 .. s (one tensor per operand, plain schedule
+// in the kernel's causal tile order; ws is not used).
 int run_attention(const void* q, const void* k, const void* v, const void* const* shards, int P,
                   const xs::EpiParams& epi, int B, int S, int H, int D, float scale, void* ws, size_t ws_bytes,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, bool causal = false) {
     DeviceInfo dev;
     int rc = device_info(&dev);
     if (rc != XS_OK) return rc;
     const Plan pl = make_plan(B, S, H, D, dev);
-    const bool split = ws != nullptr && pl.split;
+    const bool split = !causal && ws != nullptr && pl.split;
     if (split && ws_bytes < pl.ws_bytes) return XS_ERR_WORKSPACE;
     xs::AttnArgs a;
     std::memset(&a, 0, sizeof a);
@@ -299,8 +301,12 @@ int run_attention(const void* q, const void* k, const void* v, const void* const
         if ((rc = encode_bshd(&tq, q, B, S, H, D)) != XS_OK) return rc;
         if ((rc = encode_bshd(&tk, k, B, S, H, D)) != XS_OK) return rc;
         if ((rc = encode_bshd(&tv, v, B, S, H, D)) != XS_OK) return rc;
-        e = (D == 128) ? xs::launch_attn<128>(tq, tk, tv, a, grid, split, stream)
-                       : xs::launch_attn<64>(tq, tk, tv, a, grid, split, stream);
+        if (causal)
+            e = (D == 128) ? xs::launch_attn_causal<128>(tq, tk, tv, a, grid, stream)
+                           : xs::launch_attn_causal<64>(tq, tk, tv, a, grid, stream);
+        else
+            e = (D == 128) ? xs::launch_attn<128>(tq, tk, tv, a, grid, split, stream)
+                           : xs::launch_attn<64>(tq, tk, tv, a, grid, split, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return XS_OK;
@@ -455,6 +461,22 @@ int xs_attn_fwd_balanced_noalloc(const void* q, const void* k, const void* v, in
     if ((rc = noalloc_scratch(&scratch)) != XS_OK) return rc;
     return attn_layout_call(q, k, v, layout, outs, B, S, H, D, P, scale, scratch, NOALLOC_SCRATCH_BYTES,
                             static_cast<cudaStream_t>(stream));
+}
+
+int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, void* const* outs, int B, int S,
+                       int H, int D, int P, float scale, void* stream) {
+    if (!outs) return XS_ERR_NULL;
+    xs::EpiParams epi;
+    int n_out = 0;
+    int64_t out_bytes = 0;
+    bool need_div = false;
+    int rc = layout_epi(layout, outs, B, S, H, D, P, &epi, &n_out, &out_bytes, &need_div);
+    if (rc != XS_OK) return rc;
+    rc = validate_attn(q, k, v, outs, n_out, B, S, H, D, layout == XS_LAYOUT_CONTIGUOUS ? 1 : P, scale, out_bytes,
+                       need_div);
+    if (rc != XS_OK) return rc;
+    return run_attention(q, k, v, nullptr, 0, epi, B, S, H, D, scale, nullptr, 0, static_cast<cudaStream_t>(stream),
+                         true);
 }
 
 int xs_attn_ulysses_fwd(const void* const* q_shards, const void* const* k_shards, const void* const* v_shards,

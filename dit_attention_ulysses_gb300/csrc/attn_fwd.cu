@@ -203,9 +203,33 @@ __device__ __forceinline__ long long sk_start(const AttnArgs& a, int i) {
 // key-block iterations (CTAs from sk_ctas on have none).  A range holds at most
 // one part (its first piece, when it starts inside a tile) and at most one head
 // (its last piece, when it ends inside a tile that it entered at block 0).
+//
+// CAUSAL: query tile qt needs key blocks 0 .. qt only, so tiles differ in
+// length.  They run whole, longest first (query tiles in descending order, the
+// B*H tiles of one query tile side by side), dealt out in waves of one tile per
+// CTA in snake order: CTAs 0 .. G-1 in even waves, G-1 .. 0 in odd ones, so
+// that the CTA given the longest tile of a wave gets the shortest of the next.
+// The sequence of a CTA ends at the first index past the last tile, since the
+// tile index grows with idx.
+template <bool CAUSAL>
 __device__ __forceinline__ bool get_work(const AttnArgs& a, int idx, Work& w) {
     const int G = static_cast<int>(gridDim.x);
     const int i = static_cast<int>(blockIdx.x);
+    if constexpr (CAUSAL) {
+        const long long u = static_cast<long long>(idx) * G + ((idx & 1) ? G - 1 - i : i);
+        if (u >= a.units) return false;
+        const int bhs = a.B * a.H;
+        const int t = static_cast<int>(u);
+        const int bh = t % bhs;
+        w.qt = a.n_qt - 1 - t / bhs;
+        w.h = bh % a.H;
+        w.b = bh / a.H;
+        w.k0 = 0;
+        w.nb = w.qt + 1;
+        w.kind = WORK_FULL;
+        w.t_sk = -1;
+        return true;
+    }
     const int n = a.n_kv;
     const int dp = a.sp.dp_tiles;
     const int ndp = dp > i ? (dp - i + G - 1) / G : 0;
@@ -280,7 +304,7 @@ __device__ __forceinline__ const CUtensorMap* pick_map(const AttnArgs& a, const 
 }
 
 // Run by one thread.
-template <int D>
+template <int D, bool CAUSAL>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               const AttnArgs& a, uint8_t* smem, uint32_t bar0, volatile int* abort_flag) {
     using C = Cfg<D>;
@@ -291,7 +315,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     int q_last = -1;          // u_iter of the last Q load issued
     bool ok = true;
     Work w;
-    for (; ok && get_work(a, u_iter, w); ++u_iter) {
+    for (; ok && get_work<CAUSAL>(a, u_iter, w); ++u_iter) {
         const int b = w.b, h = w.h, qt = w.qt;
         const int qb = u_iter % C::Q_BUFS;
         if (u_iter >= C::Q_BUFS)
@@ -307,7 +331,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         {   // start the next piece's Q towards L2: its load waits for this piece's
             // last S MMA (one Q buffer at D = 128) and then hits L2, not HBM
             Work wn;
-            if (get_work(a, u_iter + 1, wn)) {
+            if (get_work<CAUSAL>(a, u_iter + 1, wn)) {
                 int r;
                 const CUtensorMap* m = pick_map(a, tq, wn.qt * BLOCK_M, r);
                 for (int pnl = 0; pnl < C::PANELS; ++pnl) tma_prefetch_l2_4d(m, pnl * 64, wn.h, r, wn.b);
@@ -358,7 +382,7 @@ __device__ __forceinline__ constexpr uint32_t k_step16(int kk) {
 __device__ __forceinline__ constexpr uint32_t v_step16(int kk) { return static_cast<uint32_t>(kk * (2048 >> 4)); }
 
 // Issuer of S(j) = Q K_j^T (SS) into S buffer (block index) & 1.  One thread.
-template <int D>
+template <int D, bool CAUSAL>
 __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
                            volatile int* abort_flag) {
     using C = Cfg<D>;
@@ -372,7 +396,7 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
     int u_iter = 0;
     bool ok = true;
     Work w;
-    for (; ok && get_work(a, u_iter, w); ++u_iter) {
+    for (; ok && get_work<CAUSAL>(a, u_iter, w); ++u_iter) {
         const int n = w.nb;
         const int qb = u_iter % C::Q_BUFS;
         const uint64_t qdesc = desc_add(qdesc0, qb * (C::TILE_BYTES >> 4));
@@ -407,7 +431,7 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
 }
 
 // Issuer of PV(j): O += P(j) V_j (A = P buffer from TMEM).  One thread.
-template <int D>
+template <int D, bool CAUSAL>
 __device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
                             volatile int* abort_flag) {
     using C = Cfg<D>;
@@ -420,7 +444,7 @@ __device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uin
     int u_iter = 0;
     bool ok = true;
     Work w;
-    for (; ok && get_work(a, u_iter, w); ++u_iter) {
+    for (; ok && get_work<CAUSAL>(a, u_iter, w); ++u_iter) {
         const int n = w.nb;
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gj = g + j;
@@ -605,7 +629,7 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
     return true;
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
                              volatile int* abort_flag) {
     using C = Cfg<D>;
@@ -635,9 +659,14 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
         int n, valid0;   // only these two stay live through the block loop
         {
             Work w;
-            if (!get_work(a, u_iter, w)) break;
+            if (!get_work<CAUSAL>(a, u_iter, w)) break;
             n = w.nb;
-            valid0 = a.S - w.k0 * BLOCK_N;
+            // key columns of the piece this row attends to: keys below S, and
+            // (causal) keys up to the row's own position
+            if constexpr (CAUSAL)
+                valid0 = min(a.S, w.qt * BLOCK_M + row + 1) - w.k0 * BLOCK_N;
+            else
+                valid0 = a.S - w.k0 * BLOCK_N;
         }
         float m_run = 0.0f, l_run = 0.0f;
         for (int j = 0; j < n; ++j, ++g) {
@@ -652,7 +681,11 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
             tc_fence_before();
             warp_arrive(bar(C::B_S_FREE + sb));  // the MMA may now overwrite this S buffer
             const int valid = valid0 - j * BLOCK_N;
-            const bool tail = valid < BLOCK_N;
+            // Warp-uniform whenever the tail is (no causal mask).  On the causal
+            // diagonal block the rows of a warp differ, and one vote keeps the
+            // warp on one path (columns at or past `valid` are masked either way).
+            bool tail = valid < BLOCK_N;
+            if constexpr (CAUSAL) tail = __any_sync(0xffffffffu, tail);
             if (tail) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q)
@@ -722,7 +755,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
         if (!ok) break;
         const float l_row = xsum[row] + xsum[BLOCK_M + row];
         Work w;
-        get_work(a, u_iter, w);   // the same piece of work as above (recomputed, not kept live)
+        get_work<CAUSAL>(a, u_iter, w);   // the same piece of work as above (recomputed, not kept live)
         const int b = w.b, h = w.h, qt = w.qt;
         ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns);
         if (!ok) break;
@@ -782,7 +815,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
 
 // The whole kernel; tq, tk, tv point to one tensor map each, or to n_maps maps
 // (one per input sequence shard, args.in_Sl != 0).
-template <int D>
+template <int D, bool CAUSAL>
 __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                                           int n_maps, const AttnArgs& args) {
     using C = Cfg<D>;
@@ -828,15 +861,15 @@ __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorM
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < 8) {
-        softmax_role<D>(args, smem, bar0, tmem_base, abort_flag);
+        softmax_role<D, CAUSAL>(args, smem, bar0, tmem_base, abort_flag);
     } else if (lane_id() == 0) {
         // single-thread roles; the other lanes of these warps wait at the end
         if (warp == WARP_TMA)
-            producer_role<D>(tq, tk, tv, args, smem, bar0, abort_flag);
+            producer_role<D, CAUSAL>(tq, tk, tv, args, smem, bar0, abort_flag);
         else if (warp == WARP_MMA_S)
-            mma_s_role<D>(args, smem, bar0, tmem_base, abort_flag);
+            mma_s_role<D, CAUSAL>(args, smem, bar0, tmem_base, abort_flag);
         else if (warp == WARP_MMA_PV)
-            mma_pv_role<D>(args, smem, bar0, tmem_base, abort_flag);
+            mma_pv_role<D, CAUSAL>(args, smem, bar0, tmem_base, abort_flag);
     }
     __syncwarp();
 
@@ -850,7 +883,7 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_a2a_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ AttnArgs args) {
-    attn_body<D>(&tmap_q, &tmap_k, &tmap_v, 1, args);
+    attn_body<D, false>(&tmap_q, &tmap_k, &tmap_v, 1, args);
 }
 
 // Q, K, V read straight from the P sequence shards of the Ulysses ranks: the
@@ -860,7 +893,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_ulysses_kernel(const __grid_constant__ AttnArgs args, const __grid_constant__ ShardMaps maps) {
-    attn_body<D>(maps.q, maps.k, maps.v, args.S / args.in_Sl, args);
+    attn_body<D, false>(maps.q, maps.k, maps.v, args.S / args.in_Sl, args);
+}
+
+// Causal attention (row s attends to keys 0 .. s), one [B, S, H, D] tensor per
+// operand; the tile order and key-block counts are get_work's causal ones.
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_causal_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ AttnArgs args) {
+    attn_body<D, true>(&tmap_q, &tmap_k, &tmap_v, 1, args);
 }
 
 }  // namespace
@@ -910,6 +952,20 @@ cudaError_t launch_attn_sharded(const ShardMaps& maps, int P, const AttnArgs& ar
                                        Cfg<D>::SMEM_ALLOC, stream);
 }
 
+template <int D>
+cudaError_t launch_attn_causal(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const AttnArgs& args, int grid, cudaStream_t stream) {
+    auto kern = attn_causal_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, args);
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_attn_causal<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                            const AttnArgs&, int, cudaStream_t);
+template cudaError_t launch_attn_causal<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                             const AttnArgs&, int, cudaStream_t);
 template cudaError_t launch_attn_sharded<64>(const ShardMaps&, int, const AttnArgs&, int, bool, cudaStream_t);
 template cudaError_t launch_attn_sharded<128>(const ShardMaps&, int, const AttnArgs&, int, bool, cudaStream_t);
 template int attn_smem_bytes<64>();

@@ -74,6 +74,12 @@ template <int D>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnArgs& args, int grid, bool cooperative, cudaStream_t stream);
 
+// Causal attention (row s attends to keys 0 .. s): tiles run whole, longest
+// first (args.sp is ignored; no workspace, no co-residency needed).
+template <int D>
+cudaError_t launch_attn_causal(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const AttnArgs& args, int grid, cudaStream_t stream);
+
 // The same kernel reading Q, K, V from P sequence shards (args.in_Sl = S / P).
 template <int D>
 cudaError_t launch_attn_sharded(const ShardMaps& maps, int P, const AttnArgs& args, int grid, bool cooperative,

@@ -259,6 +259,28 @@ int xs_attn_fwd_balanced_noalloc(const void* q, const void* k, const void* v, in
                                  int B, int S, int H, int D, int P, float scale, void* stream);
 
 /*
+ * xs_attn_causal_fwd -- causal attention with the same fused output layouts:
+ *     O[b,s,h,:] = sum_{t<=s} exp(x_t - m) V[b,t,h,:] / sum_{t<=s} exp(x_t - m),
+ *     x_t = scale * <Q[b,s,h,:], K[b,t,h,:]>,  m = max_{t<=s} x_t,
+ * i.e. query row s attends to keys 0 .. s only.  The X-Stage pages treat
+ * bidirectional DiT attention and define no masked form; this variant is the
+ * masked self-attention of autoregressive models, with the epilogue stores of
+ * the fused Ulysses layout unchanged.
+ *   layout  XS_LAYOUT_A2A (outs = P sequence shards [B, S/P, H, D]),
+ *           XS_LAYOUT_CONTIGUOUS (outs[0] = one [B, S, H, D] tensor, P ignored)
+ *           or XS_LAYOUT_HEADS (outs = P head shards [B, S, H/P, D]); the same
+ *           buffers, ownership and checks as xs_attn_a2a_fwd, xs_attn_fwd and
+ *           xs_attn_heads_fwd.
+ * Query tile t (rows [128t, 128t + 128)) reads key blocks 0 .. t; the block on
+ * the diagonal is masked per row.  Tiles are scheduled longest first over all
+ * SMs; no workspace is used.  The three layouts are bit-identical to each
+ * other.  Returns as xs_attn_a2a_fwd (XS_ERR_LAYOUT for an unknown layout);
+ * asynchronous on `stream`.
+ */
+int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, void* const* outs,
+                       int B, int S, int H, int D, int P, float scale, void* stream);
+
+/*
  * xs_burst_gap -- Burst-Gap microbenchmark of the store path the fused epilogue
  * uses (SM -> L2 -> HBM on one GPU).  X-Stage (arXiv 2607.23264), gist.science
  * technical summary, "Methodology: The X-Stage Abstraction and Burst-Gap

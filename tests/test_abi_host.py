@@ -155,6 +155,23 @@ def test_balanced_validation(xs):
                                     None) == xs.XS_ERR_OVERLAP
 
 
+def test_causal_validation(xs):
+    lib = xs.lib
+    outs = _outs(2)
+    A2A, CONT, HEADS = xs.XS_LAYOUT_A2A, xs.XS_LAYOUT_CONTIGUOUS, xs.XS_LAYOUT_HEADS
+    assert lib.xs_attn_causal_fwd(Q, K, V, 7, outs, 1, 256, 2, 64, 2, 0.1, None) == xs.XS_ERR_LAYOUT
+    assert lib.xs_attn_causal_fwd(Q, K, V, A2A, None, 1, 256, 2, 64, 2, 0.1, None) == xs.XS_ERR_NULL
+    assert lib.xs_attn_causal_fwd(None, K, V, A2A, outs, 1, 256, 2, 64, 2, 0.1, None) == xs.XS_ERR_NULL
+    assert lib.xs_attn_causal_fwd(Q, K, V, A2A, outs, 1, 256, 3, 64, 2, 0.1, None) == xs.XS_ERR_DIVISIBILITY
+    assert lib.xs_attn_causal_fwd(Q, K, V, HEADS, outs, 1, 255, 2, 64, 2, 0.1, None) == xs.XS_ERR_DIVISIBILITY
+    assert lib.xs_attn_causal_fwd(Q, K, V, A2A, outs, 1, 256, 2, 96, 2, 0.1, None) == xs.XS_ERR_HEAD_DIM
+    assert lib.xs_attn_causal_fwd(Q, K, V, A2A, outs, 0, 256, 2, 64, 2, 0.1, None) == xs.XS_ERR_SHAPE
+    assert lib.xs_attn_causal_fwd(Q, K, V, A2A, outs, 1, 256, 2, 64, 2, float("nan"), None) == xs.XS_ERR_SCALE
+    assert lib.xs_attn_causal_fwd(Q + 8, K, V, A2A, outs, 1, 256, 2, 64, 2, 0.1, None) == xs.XS_ERR_ALIGNMENT
+    assert lib.xs_attn_causal_fwd(Q, K, V, CONT, _outs(1, base=V + 4096), 1, 256, 2, 64, 1, 0.1, None) == \
+        xs.XS_ERR_OVERLAP
+
+
 def test_workspace_query_validation(xs):
     import ctypes
     lib = xs.lib
