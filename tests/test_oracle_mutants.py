@@ -13,6 +13,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_causal_pins as cpins
 import test_oracle_pins as pins
 
 MUTANTS = {
@@ -31,6 +32,27 @@ MUTANTS = {
     "head shard takes the wrong head": ("o[idx4(b, s, r * Hl + j, d, S, H, D)];",
                                         "o[idx4(b, s, j * P + r, d, S, H, D)];"),
 }
+
+# Mistakes in the causal key window (row i must see keys 0 .. i), caught by the
+# causal pins of test_oracle_causal_pins.
+CAUSAL_SITE = "return causal ? i + 1 : S;"
+CAUSAL_MUTANTS = {
+    "causal window one key short": "return causal ? (i > 0 ? i : 1) : S;",
+    "causal window one key long": "return causal ? (i + 2 < S ? i + 2 : S) : S;",
+    "causal window counted from the end": "return causal ? S - i : S;",
+    "causal flag ignored": "return S;",
+}
+
+CAUSAL_PIN_CASES = [
+    (cpins.test_causal_worked_example_by_hand, ()),
+    (cpins.test_causal_first_row_copies_first_value_row, (5,)),
+    (cpins.test_causal_q_zero_gives_prefix_means_of_v, (7,)),
+    (cpins.test_causal_last_row_equals_bidirectional, ()),
+    (cpins.test_causal_future_keys_and_values_do_not_matter, ()),
+    (cpins.test_causal_weights_vanish_above_the_diagonal_and_sum_to_one, ()),
+    (cpins.test_causal_brute_force_numpy, (8,)),
+    (cpins.test_causal_torch_sdpa_fp64_crosscheck, ()),
+]
 
 PIN_CASES = [
     (pins.test_worked_example_by_hand, ()),
@@ -72,13 +94,29 @@ def test_pins_catch_mutant(name, tmp_path, monkeypatch):
     assert failures, f"no pin caught the mutant {name!r}"
 
 
+@pytest.mark.parametrize("name", sorted(CAUSAL_MUTANTS))
+def test_causal_pins_catch_mutant(name, tmp_path, monkeypatch):
+    lib_path = _build_mutant(tmp_path, name, CAUSAL_SITE, CAUSAL_MUTANTS[name])
+    monkeypatch.setattr(oracle, "_LIB", lib_path)
+    monkeypatch.setattr(oracle, "_SRC", lib_path)
+    monkeypatch.setattr(oracle, "_lib", None)
+    failures = []
+    for fn, args in CAUSAL_PIN_CASES:
+        try:
+            fn(*args)
+        except (AssertionError, RuntimeError):
+            failures.append(fn.__name__)
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert failures, f"no causal pin caught the mutant {name!r}"
+
+
 def test_unmutated_copy_passes_all_pins(tmp_path, monkeypatch):
     src = open(oracle._SRC).read()
     lib_path = _build_mutant(tmp_path, "identity", "double m = -INFINITY;", "double m = -INFINITY;")
     monkeypatch.setattr(oracle, "_LIB", lib_path)
     monkeypatch.setattr(oracle, "_SRC", lib_path)
     monkeypatch.setattr(oracle, "_lib", None)
-    for fn, args in PIN_CASES:
+    for fn, args in PIN_CASES + CAUSAL_PIN_CASES:
         fn(*args)
     monkeypatch.setattr(oracle, "_lib", None)
     assert "double m = -INFINITY;" in src
