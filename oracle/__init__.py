@@ -14,6 +14,7 @@ itself; the oracle takes the textbook definition O = softmax(Q K^T * scale) V,
 non-causal, no mask, no bias, fp64 throughout (see ``attention_oracle.c``).
 ``causal=True`` selects the causal variant, which the pages do not treat: row i
 attends to keys 0 .. i only (plain attention over the first i + 1 keys).
+``attention_varlen`` applies either form to each of several packed sequences.
 
 Every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py`` (brute force, closed forms, invariants, an exact
@@ -180,6 +181,28 @@ def attention_a2a(q, k, v, scale: float, P: int, nthreads: int | None = None, ca
     Returns the P output shards as one array [P, B, S/P, H, D] (float64).
     """
     return a2a(head_shards(attention(q, k, v, scale, nthreads, causal), P))
+
+
+def attention_varlen(q, k, v, seqlens, scale: float, causal: bool = False,
+                     nthreads: int | None = None) -> np.ndarray:
+    """Attention of packed variable-length sequences (not on the pages; the packed
+    batches of variable-length attention kernels): q, k, v are [1, T, H, D] bf16
+    bits holding sequences of lengths ``seqlens`` back to back (T = sum of them),
+    and every query row attends only to the keys of its own sequence (causal: of
+    its own sequence and at or before its own position).  Computed as exact
+    attention of each sequence's slice on its own.  Returns [1, T, H, D] float64."""
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    lens = [int(n) for n in seqlens]
+    if q.ndim != 4 or q.shape[0] != 1 or any(n < 0 for n in lens) or sum(lens) != q.shape[1]:
+        raise ValueError("packed inputs are [1, T, H, D] with T = sum(seqlens), seqlens >= 0")
+    o = np.empty(q.shape, dtype=np.float64)
+    start = 0
+    for n in lens:
+        if n:
+            sl = slice(start, start + n)
+            o[:, sl] = attention(q[:, sl], k[:, sl], v[:, sl], scale, nthreads, causal)
+        start += n
+    return o
 
 
 def _exact_bf16_bits(x: np.ndarray) -> np.ndarray:

@@ -15,6 +15,7 @@ import pytest
 import oracle
 import test_oracle_causal_pins as cpins
 import test_oracle_pins as pins
+import test_oracle_varlen_pins as vpins
 
 MUTANTS = {
     "scale dropped": ("x[j] = scale * dot;", "x[j] = dot;"),
@@ -110,13 +111,56 @@ def test_causal_pins_catch_mutant(name, tmp_path, monkeypatch):
     assert failures, f"no causal pin caught the mutant {name!r}"
 
 
+# Mistakes in the packed variable-length form (a Python function over the C
+# row routine), planted by wrapping the committed function.
+_varlen = oracle.attention_varlen
+
+
+def _boundary_shifted(q, k, v, seqlens, scale, causal=False, nthreads=None):
+    lens = list(seqlens)
+    i = next((j for j in range(len(lens) - 1) if lens[j] > 1), None)
+    if i is not None:   # first boundary one row late
+        lens[i] -= 1
+        lens[i + 1] += 1
+    return _varlen(q, k, v, lens, scale, causal, nthreads)
+
+
+VARLEN_MUTANTS = {
+    "boundary one row off": _boundary_shifted,
+    "rows attend across sequences": lambda q, k, v, seqlens, scale, causal=False, nthreads=None:
+        _varlen(q, k, v, [sum(seqlens)], scale, causal, nthreads),
+    "causal flag dropped": lambda q, k, v, seqlens, scale, causal=False, nthreads=None:
+        _varlen(q, k, v, seqlens, scale, False, nthreads),
+}
+
+VARLEN_PIN_CASES = [
+    (vpins.test_varlen_worked_example_by_hand, (True,)),
+    (vpins.test_varlen_brute_force_numpy, ([5, 1, 7], True)),
+    (vpins.test_varlen_torch_sdpa_fp64_crosscheck, (False,)),
+    (vpins.test_varlen_other_and_empty_sequences_do_not_matter, ()),
+    (vpins.test_varlen_q_zero_gives_sequence_means, (True,)),
+]
+
+
+@pytest.mark.parametrize("name", sorted(VARLEN_MUTANTS))
+def test_varlen_pins_catch_mutant(name, monkeypatch):
+    monkeypatch.setattr(oracle, "attention_varlen", VARLEN_MUTANTS[name])
+    failures = []
+    for fn, args in VARLEN_PIN_CASES:
+        try:
+            fn(*args)
+        except AssertionError:
+            failures.append(fn.__name__)
+    assert failures, f"no varlen pin caught the mutant {name!r}"
+
+
 def test_unmutated_copy_passes_all_pins(tmp_path, monkeypatch):
     src = open(oracle._SRC).read()
     lib_path = _build_mutant(tmp_path, "identity", "double m = -INFINITY;", "double m = -INFINITY;")
     monkeypatch.setattr(oracle, "_LIB", lib_path)
     monkeypatch.setattr(oracle, "_SRC", lib_path)
     monkeypatch.setattr(oracle, "_lib", None)
-    for fn, args in PIN_CASES + CAUSAL_PIN_CASES:
+    for fn, args in PIN_CASES + CAUSAL_PIN_CASES + VARLEN_PIN_CASES:
         fn(*args)
     monkeypatch.setattr(oracle, "_lib", None)
     assert "double m = -INFINITY;" in src
