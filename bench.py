@@ -292,6 +292,20 @@ def run_ours(args, rank, world, local_rank):
     def causal():
         xs.xs_attn_causal_fwd(q, k, v, xs.XS_LAYOUT_A2A, causal_out, w.scale, stream)
 
+    # packed variable-length sequences: the same B*S tokens as a seeded mix of lengths
+    # between (B*S)/16 and (B*S)/2 (the last one cut to fit), bidirectional within each
+    T = B * S
+    rng = np.random.default_rng(12345)
+    seqlens = []
+    while sum(seqlens) < T:
+        seqlens.append(int(rng.integers(max(1, T // 16), max(2, T // 2))))
+    seqlens[-1] -= sum(seqlens) - T
+    q_p, k_p, v_p = (x.view(T, H, D) for x in (q, k, v))
+    varlen_out = [torch.empty((T // P, H, D), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+
+    def varlen():
+        xs.xs_attn_varlen_fwd(q_p, k_p, v_p, seqlens, xs.XS_LAYOUT_A2A, varlen_out, w.scale, False, stream)
+
     for _ in range(max(3, args.warmup)):
         fused()
     torch.cuda.synchronize()
@@ -322,15 +336,16 @@ def run_ours(args, rank, world, local_rank):
     # ablation: attention alone (contiguous store), fused, and attention + separate
     # re-layout, interleaved run by run so that clock drift affects all three alike
     n_abl = max(10, min(args.steps, 50))
-    for fn in (alone, serial_path, causal) + ((ulysses_fused, ulysses_serial) if uly else ()):
+    for fn in (alone, serial_path, causal, varlen) + ((ulysses_fused, ulysses_serial) if uly else ()):
         for _ in range(3):
             fn()
-    ta, tf, ts, tc, tuf, tus = [], [], [], [], [], []
+    ta, tf, ts, tc, tv, tuf, tus = [], [], [], [], [], [], []
     for _ in range(n_abl):
         ta += time_steps(torch, alone, 1, flush, stream)
         tf += time_steps(torch, fused, 1, flush, stream)
         ts += time_steps(torch, serial_path, 1, flush, stream)
         tc += time_steps(torch, causal, 1, flush, stream)
+        tv += time_steps(torch, varlen, 1, flush, stream)
         if uly:
             tuf += time_steps(torch, ulysses_fused, 1, flush, stream)
             tus += time_steps(torch, ulysses_serial, 1, flush, stream)
@@ -341,6 +356,12 @@ def run_ours(args, rank, world, local_rank):
     causal_line = {"api": "xs_attn_causal_fwd", "ms": t_causal, "tflops": causal_flops / (t_causal * 1e-3) / 1e12,
                    "flops": causal_flops, "flops_rule": "4*B*H*D*S*(S+1)/2 (unmasked query-key pairs)",
                    "over_bidirectional_fused_ms": t_causal / t_fused, "runs": n_abl, "statistic": "median"}
+    varlen_flops = 4 * H * D * sum(n * n for n in seqlens)
+    t_varlen = statistics.median(tv)
+    varlen_line = {"api": "xs_attn_varlen_fwd", "seqlens": seqlens, "ms": t_varlen,
+                   "tflops": varlen_flops / (t_varlen * 1e-3) / 1e12, "flops": varlen_flops,
+                   "flops_rule": "4*H*D*sum(len^2) (each sequence attends to itself)",
+                   "runs": n_abl, "statistic": "median"}
     ulysses = None
     if uly:
         t_uf, t_us = statistics.median(tuf), statistics.median(tus)
@@ -398,6 +419,7 @@ def run_ours(args, rank, world, local_rank):
                 "ms_per_step": e2e_ms, "api": "xs_attn_a2a_fwd_staged"},
         "ulysses_step": ulysses,
         "causal": causal_line,
+        "varlen": varlen_line,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),

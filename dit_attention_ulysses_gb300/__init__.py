@@ -33,6 +33,7 @@ __all__ = [
     "xs_attn_fwd_balanced",
     "xs_attn_fwd_balanced_noalloc",
     "xs_attn_causal_fwd",
+    "xs_attn_varlen_fwd",
     "Workspace",
     "xs_attn_get_device_error",
     "xs_attn_error_string",
@@ -83,6 +84,8 @@ EXPORTS = {
                                             _f32, _vp]),
     "xs_attn_causal_fwd": (_int, [_vp, _vp, _vp, _int, ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32,
                                   _vp]),
+    "xs_attn_varlen_fwd": (_int, [_vp, _vp, _vp, ctypes.POINTER(_int), _int, _int, _int, ctypes.POINTER(_vp), _int,
+                                  _int, _int, _int, _f32, _vp]),
     "xs_attn_ulysses_fwd": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                    ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32, _vp, _size, _vp]),
     "xs_relayout_a2a_inverse": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int, _int, _int, _int,
@@ -307,6 +310,29 @@ def xs_attn_causal_fwd(q, k, v, layout: int, outs, scale: float, stream=None) ->
     _check(lib.xs_attn_causal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), layout,
                                   _ptr_array([o.data_ptr() for o in os_]), B, S, H, D, len(os_), scale,
                                   _stream_handle(stream)), "xs_attn_causal_fwd")
+
+
+def _thd(t, name):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+        raise TypeError(f"{name} must be a contiguous CUDA bfloat16 tensor [T,H,D]")
+    return t
+
+
+def xs_attn_varlen_fwd(q, k, v, seqlens, layout: int, outs, scale: float, causal: bool = False,
+                       stream=None) -> None:
+    """Attention over packed variable-length sequences: ``q``, ``k``, ``v`` are
+    [T, H, D] bf16 holding sequences of lengths ``seqlens`` (host integers) back to
+    back; each row attends to its own sequence (``causal``: up to its own position).
+    ``layout`` XS_LAYOUT_A2A (P shards [T/P, H, D]), XS_LAYOUT_CONTIGUOUS (one
+    [T, H, D] tensor) or XS_LAYOUT_HEADS (P head shards [T, H/P, D])."""
+    T, H, D = _thd(q, "q").shape
+    _thd(k, "k"), _thd(v, "v")
+    os_ = [_thd(o, "out") for o in outs]
+    lens = (ctypes.c_int * max(1, len(seqlens)))(*[int(n) for n in seqlens])
+    _check(lib.xs_attn_varlen_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), lens, len(seqlens), int(bool(causal)),
+                                  layout, _ptr_array([o.data_ptr() for o in os_]), T, H, D, len(os_), scale,
+                                  _stream_handle(stream)), "xs_attn_varlen_fwd")
 
 
 def attn_a2a(q, k, v, P: int, scale: float | None = None, stream=None, workspace=None):

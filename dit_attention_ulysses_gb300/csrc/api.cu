@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <cmath>
@@ -477,6 +478,69 @@ int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, 
     if (rc != XS_OK) return rc;
     return run_attention(q, k, v, nullptr, 0, epi, B, S, H, D, scale, nullptr, 0, static_cast<cudaStream_t>(stream),
                          true);
+}
+
+int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* seqlens, int n_seqs, int causal,
+                       int layout, void* const* outs, int T, int H, int D, int P, float scale, void* stream) {
+    if (!outs || !seqlens) return XS_ERR_NULL;
+    if (n_seqs < 1 || n_seqs > xs::MAX_VARLEN_SEQS) return XS_ERR_SHAPE;
+    int64_t total = 0, tiles = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+        if (seqlens[i] < 0 || seqlens[i] > 65536 * 128) return XS_ERR_SHAPE;
+        total += seqlens[i];
+        tiles += (seqlens[i] + 127) / 128;
+    }
+    if (total != T || tiles > xs::MAX_VARLEN_TILES) return XS_ERR_SHAPE;
+    xs::EpiParams epi;
+    int n_out = 0;
+    int64_t out_bytes = 0;
+    bool need_div = false;
+    int rc = layout_epi(layout, outs, 1, T, H, D, P, &epi, &n_out, &out_bytes, &need_div);
+    if (rc != XS_OK) return rc;
+    rc = validate_attn(q, k, v, outs, n_out, 1, T, H, D, layout == XS_LAYOUT_CONTIGUOUS ? 1 : P, scale, out_bytes,
+                       need_div);
+    if (rc != XS_OK) return rc;
+    DeviceInfo dev;
+    if ((rc = device_info(&dev)) != XS_OK) return rc;
+
+    // The tile list, longest first: tile (i, t) reads ceil(len_i / 128) key blocks,
+    // or t + 1 when causal; ties keep sequence order, then query-tile order.
+    static thread_local xs::VarlenTable vt;   // 20 KB: kept off the stack
+    vt.n_seqs = n_seqs;
+    vt.cu[0] = 0;
+    for (int i = 0; i < n_seqs; ++i) vt.cu[i + 1] = vt.cu[i] + seqlens[i];
+    int n = 0;
+    for (int i = 0; i < n_seqs; ++i)
+        for (int t = 0; t * 128 < seqlens[i]; ++t) vt.tile[n++] = (static_cast<unsigned>(i) << 16) | static_cast<unsigned>(t);
+    vt.n_tiles = n;
+    auto blocks = [&](unsigned e) {
+        const int i = static_cast<int>(e >> 16), t = static_cast<int>(e & 0xffffu);
+        return causal ? t + 1 : (seqlens[i] + 127) / 128;
+    };
+    std::stable_sort(vt.tile, vt.tile + n, [&](unsigned x, unsigned y) { return blocks(x) > blocks(y); });
+
+    xs::AttnArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.B = 1;
+    a.S = T;
+    a.H = H;
+    a.n_kv = (T + 127) / 128;
+    a.n_qt = (T + 127) / 128;
+    a.units = n * H;
+    a.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.epi = epi;
+    a.timeout_ns = timeout_ns();
+    a.sp.dp_tiles = a.units;
+    const int grid = a.units < dev.sms ? a.units : dev.sms;
+    CUtensorMap tq, tk, tv;
+    if ((rc = encode_bshd(&tq, q, 1, T, H, D)) != XS_OK) return rc;
+    if ((rc = encode_bshd(&tk, k, 1, T, H, D)) != XS_OK) return rc;
+    if ((rc = encode_bshd(&tv, v, 1, T, H, D)) != XS_OK) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = (D == 128) ? xs::launch_attn_varlen<128>(tq, tk, tv, a, vt, causal != 0, grid, st)
+                                     : xs::launch_attn_varlen<64>(tq, tk, tv, a, vt, causal != 0, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return XS_OK;
 }
 
 int xs_attn_ulysses_fwd(const void* const* q_shards, const void* const* k_shards, const void* const* v_shards,

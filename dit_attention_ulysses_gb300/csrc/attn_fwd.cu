@@ -190,6 +190,8 @@ struct Work {
                 // WORK_PART: blocks [k0, k0 + nb), k0 > 0, of a split tile,
                 // published as a partial result
     int t_sk;   // index of the tile among the split-scheduled tiles (-1: whole wave)
+    int row0;   // VARLEN: packed row of the tile's sequence start (b = 0)
+    int len;    // VARLEN: the sequence's length
 };
 
 // Start of CTA i's range of split-scheduled key-block iterations.
@@ -211,10 +213,33 @@ __device__ __forceinline__ long long sk_start(const AttnArgs& a, int i) {
 // that the CTA given the longest tile of a wave gets the shortest of the next.
 // The sequence of a CTA ends at the first index past the last tile, since the
 // tile index grows with idx.
-template <bool CAUSAL>
-__device__ __forceinline__ bool get_work(const AttnArgs& a, int idx, Work& w) {
+//
+// VARLEN: packed sequences (B = 1, S = their total length).  vt->tile lists the
+// query tiles (sequence, query tile) longest first; unit u is entry u / H of it
+// for head u % H, dealt out in the same snake order.  A tile of sequence i
+// reads the key blocks of that sequence only: ceil(len_i / 128) of them, or
+// (CAUSAL) qt + 1.
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* vt, int idx, Work& w) {
     const int G = static_cast<int>(gridDim.x);
     const int i = static_cast<int>(blockIdx.x);
+    if constexpr (VARLEN) {
+        const long long u = static_cast<long long>(idx) * G + ((idx & 1) ? G - 1 - i : i);
+        if (u >= a.units) return false;
+        const int t = static_cast<int>(u) / a.H;
+        w.h = static_cast<int>(u) - t * a.H;
+        const unsigned e = vt->tile[t];
+        const int seq = static_cast<int>(e >> 16);
+        w.qt = static_cast<int>(e & 0xffffu);
+        w.b = 0;
+        w.row0 = vt->cu[seq];
+        w.len = vt->cu[seq + 1] - w.row0;
+        w.k0 = 0;
+        w.nb = CAUSAL ? w.qt + 1 : (w.len + BLOCK_N - 1) / BLOCK_N;
+        w.kind = WORK_FULL;
+        w.t_sk = -1;
+        return true;
+    }
     if constexpr (CAUSAL) {
         const long long u = static_cast<long long>(idx) * G + ((idx & 1) ? G - 1 - i : i);
         if (u >= a.units) return false;
@@ -304,9 +329,10 @@ __device__ __forceinline__ const CUtensorMap* pick_map(const AttnArgs& a, const 
 }
 
 // Run by one thread.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                              const AttnArgs& a, uint8_t* smem, uint32_t bar0, volatile int* abort_flag) {
+                              const AttnArgs& a, const VarlenTable* vt, uint8_t* smem, uint32_t bar0,
+                              volatile int* abort_flag) {
     using C = Cfg<D>;
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
@@ -315,15 +341,16 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     int q_last = -1;          // u_iter of the last Q load issued
     bool ok = true;
     Work w;
-    for (; ok && get_work<CAUSAL>(a, u_iter, w); ++u_iter) {
+    for (; ok && get_work<CAUSAL, VARLEN>(a, vt, u_iter, w); ++u_iter) {
         const int b = w.b, h = w.h, qt = w.qt;
         const int qb = u_iter % C::Q_BUFS;
         if (u_iter >= C::Q_BUFS)
             ok = thread_wait(bar(C::B_Q_FREE + qb), ((u_iter / C::Q_BUFS) - 1) & 1, abort_flag, a.timeout_ns);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(C::B_Q_FULL + qb), C::TILE_BYTES);
+        const int row_base = VARLEN ? w.row0 : 0;   // packed row of the sequence start
         int q_row;
-        const CUtensorMap* q_map = pick_map(a, tq, qt * BLOCK_M, q_row);
+        const CUtensorMap* q_map = pick_map(a, tq, row_base + qt * BLOCK_M, q_row);
         for (int pnl = 0; pnl < C::PANELS; ++pnl)
             tma_load_4d(sbase + C::Q_OFF + qb * C::TILE_BYTES + pnl * PANEL_BYTES, q_map, bar(C::B_Q_FULL + qb),
                         pnl * 64, h, q_row, b);
@@ -331,9 +358,9 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         {   // start the next piece's Q towards L2: its load waits for this piece's
             // last S MMA (one Q buffer at D = 128) and then hits L2, not HBM
             Work wn;
-            if (get_work<CAUSAL>(a, u_iter + 1, wn)) {
+            if (get_work<CAUSAL, VARLEN>(a, vt, u_iter + 1, wn)) {
                 int r;
-                const CUtensorMap* m = pick_map(a, tq, wn.qt * BLOCK_M, r);
+                const CUtensorMap* m = pick_map(a, tq, (VARLEN ? wn.row0 : 0) + wn.qt * BLOCK_M, r);
                 for (int pnl = 0; pnl < C::PANELS; ++pnl) tma_prefetch_l2_4d(m, pnl * 64, wn.h, r, wn.b);
             }
         }
@@ -348,7 +375,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
             if (!ok) break;
             mbar_arrive_expect_tx(bar(C::B_KV_FULL + stage), C::TILE_BYTES);
             int kv_row;
-            const CUtensorMap* kv_map = pick_map(a, is_v ? tv : tk, blk * BLOCK_N, kv_row);
+            const CUtensorMap* kv_map = pick_map(a, is_v ? tv : tk, row_base + blk * BLOCK_N, kv_row);
             for (int pnl = 0; pnl < C::PANELS; ++pnl)
                 tma_load_4d(sbase + C::KV_OFF + stage * C::TILE_BYTES + pnl * PANEL_BYTES, kv_map,
                             bar(C::B_KV_FULL + stage), pnl * 64, h, kv_row, b);
@@ -382,9 +409,9 @@ __device__ __forceinline__ constexpr uint32_t k_step16(int kk) {
 __device__ __forceinline__ constexpr uint32_t v_step16(int kk) { return static_cast<uint32_t>(kk * (2048 >> 4)); }
 
 // Issuer of S(j) = Q K_j^T (SS) into S buffer (block index) & 1.  One thread.
-template <int D, bool CAUSAL>
-__device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
-                           volatile int* abort_flag) {
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* smem, uint32_t bar0,
+                           uint32_t tmem_base, volatile int* abort_flag) {
     using C = Cfg<D>;
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
@@ -396,7 +423,7 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
     int u_iter = 0;
     bool ok = true;
     Work w;
-    for (; ok && get_work<CAUSAL>(a, u_iter, w); ++u_iter) {
+    for (; ok && get_work<CAUSAL, VARLEN>(a, vt, u_iter, w); ++u_iter) {
         const int n = w.nb;
         const int qb = u_iter % C::Q_BUFS;
         const uint64_t qdesc = desc_add(qdesc0, qb * (C::TILE_BYTES >> 4));
@@ -431,9 +458,9 @@ __device__ void mma_s_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint
 }
 
 // Issuer of PV(j): O += P(j) V_j (A = P buffer from TMEM).  One thread.
-template <int D, bool CAUSAL>
-__device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
-                            volatile int* abort_flag) {
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* smem, uint32_t bar0,
+                            uint32_t tmem_base, volatile int* abort_flag) {
     using C = Cfg<D>;
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
@@ -444,7 +471,7 @@ __device__ void mma_pv_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uin
     int u_iter = 0;
     bool ok = true;
     Work w;
-    for (; ok && get_work<CAUSAL>(a, u_iter, w); ++u_iter) {
+    for (; ok && get_work<CAUSAL, VARLEN>(a, vt, u_iter, w); ++u_iter) {
         const int n = w.nb;
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gj = g + j;
@@ -629,9 +656,9 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
     return true;
 }
 
-template <int D, bool CAUSAL>
-__device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, uint32_t tmem_base,
-                             volatile int* abort_flag) {
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* smem, uint32_t bar0,
+                             uint32_t tmem_base, volatile int* abort_flag) {
     using C = Cfg<D>;
     constexpr int DH = D / 2;  // O columns owned by each of a row's two threads
     const int warp = threadIdx.x >> 5;
@@ -659,14 +686,15 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
         int n, valid0;   // only these two stay live through the block loop
         {
             Work w;
-            if (!get_work<CAUSAL>(a, u_iter, w)) break;
+            if (!get_work<CAUSAL, VARLEN>(a, vt, u_iter, w)) break;
             n = w.nb;
             // key columns of the piece this row attends to: keys below S, and
             // (causal) keys up to the row's own position
+            const int seq_len = VARLEN ? w.len : a.S;
             if constexpr (CAUSAL)
-                valid0 = min(a.S, w.qt * BLOCK_M + row + 1) - w.k0 * BLOCK_N;
+                valid0 = min(seq_len, w.qt * BLOCK_M + row + 1) - w.k0 * BLOCK_N;
             else
-                valid0 = a.S - w.k0 * BLOCK_N;
+                valid0 = seq_len - w.k0 * BLOCK_N;
         }
         float m_run = 0.0f, l_run = 0.0f;
         for (int j = 0; j < n; ++j, ++g) {
@@ -755,7 +783,7 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
         if (!ok) break;
         const float l_row = xsum[row] + xsum[BLOCK_M + row];
         Work w;
-        get_work<CAUSAL>(a, u_iter, w);   // the same piece of work as above (recomputed, not kept live)
+        get_work<CAUSAL, VARLEN>(a, vt, u_iter, w);   // the same piece of work as above (recomputed, not kept live)
         const int b = w.b, h = w.h, qt = w.qt;
         ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns);
         if (!ok) break;
@@ -765,9 +793,10 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
             // 32 rows per instruction.  A 2 KB per-warp stage (32 rows x 64 B,
             // 16-byte chunks XOR-swizzled against bank conflicts) lets 4 lanes write
             // 64 contiguous bytes of a row: each store instruction covers 8 rows.
-            const int s_row = qt * BLOCK_M + row;
-            unsigned long long dst_row = 0;   // this lane's row in the destination (0: past S)
-            if (s_row < a.S) {
+            const int s_loc = qt * BLOCK_M + row;   // row within the sequence
+            unsigned long long dst_row = 0;   // this lane's row in the destination (0: past the sequence)
+            if (s_loc < (VARLEN ? w.len : a.S)) {
+                const int s_row = (VARLEN ? w.row0 : 0) + s_loc;
                 const int p = s_row / a.epi.Sl + h / a.epi.Hl;
                 const int s_dst = s_row % a.epi.Sl;
                 const int h_dst = h % a.epi.Hl;
@@ -815,9 +844,9 @@ __device__ void softmax_role(const AttnArgs& a, uint8_t* smem, uint32_t bar0, ui
 
 // The whole kernel; tq, tk, tv point to one tensor map each, or to n_maps maps
 // (one per input sequence shard, args.in_Sl != 0).
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                                          int n_maps, const AttnArgs& args) {
+                                          int n_maps, const AttnArgs& args, const VarlenTable* vt) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -861,15 +890,15 @@ __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorM
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < 8) {
-        softmax_role<D, CAUSAL>(args, smem, bar0, tmem_base, abort_flag);
+        softmax_role<D, CAUSAL, VARLEN>(args, vt, smem, bar0, tmem_base, abort_flag);
     } else if (lane_id() == 0) {
         // single-thread roles; the other lanes of these warps wait at the end
         if (warp == WARP_TMA)
-            producer_role<D, CAUSAL>(tq, tk, tv, args, smem, bar0, abort_flag);
+            producer_role<D, CAUSAL, VARLEN>(tq, tk, tv, args, vt, smem, bar0, abort_flag);
         else if (warp == WARP_MMA_S)
-            mma_s_role<D, CAUSAL>(args, smem, bar0, tmem_base, abort_flag);
+            mma_s_role<D, CAUSAL, VARLEN>(args, vt, smem, bar0, tmem_base, abort_flag);
         else if (warp == WARP_MMA_PV)
-            mma_pv_role<D, CAUSAL>(args, smem, bar0, tmem_base, abort_flag);
+            mma_pv_role<D, CAUSAL, VARLEN>(args, vt, smem, bar0, tmem_base, abort_flag);
     }
     __syncwarp();
 
@@ -883,7 +912,7 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_a2a_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ AttnArgs args) {
-    attn_body<D, false>(&tmap_q, &tmap_k, &tmap_v, 1, args);
+    attn_body<D, false, false>(&tmap_q, &tmap_k, &tmap_v, 1, args, nullptr);
 }
 
 // Q, K, V read straight from the P sequence shards of the Ulysses ranks: the
@@ -893,7 +922,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_ulysses_kernel(const __grid_constant__ AttnArgs args, const __grid_constant__ ShardMaps maps) {
-    attn_body<D, false>(maps.q, maps.k, maps.v, args.S / args.in_Sl, args);
+    attn_body<D, false, false>(maps.q, maps.k, maps.v, args.S / args.in_Sl, args, nullptr);
 }
 
 // Causal attention (row s attends to keys 0 .. s), one [B, S, H, D] tensor per
@@ -902,7 +931,18 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_causal_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ AttnArgs args) {
-    attn_body<D, true>(&tmap_q, &tmap_k, &tmap_v, 1, args);
+    attn_body<D, true, false>(&tmap_q, &tmap_k, &tmap_v, 1, args, nullptr);
+}
+
+// Packed variable-length sequences: one [1, T, H, D] tensor per operand holding
+// the sequences of vt back to back; every row attends to its own sequence
+// (CAUSAL: up to its own position).  The table travels in parameter space.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_varlen_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ AttnArgs args,
+                       const __grid_constant__ VarlenTable vt) {
+    attn_body<D, CAUSAL, true>(&tmap_q, &tmap_k, &tmap_v, 1, args, &vt);
 }
 
 }  // namespace
@@ -962,6 +1002,21 @@ cudaError_t launch_attn_causal(const CUtensorMap& tq, const CUtensorMap& tk, con
     return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_attn_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const AttnArgs& args, const VarlenTable& vt, bool causal, int grid,
+                               cudaStream_t stream) {
+    auto kern = causal ? attn_varlen_kernel<D, true> : attn_varlen_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, args, vt);
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_attn_varlen<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                            const AttnArgs&, const VarlenTable&, bool, int, cudaStream_t);
+template cudaError_t launch_attn_varlen<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                             const AttnArgs&, const VarlenTable&, bool, int, cudaStream_t);
 template cudaError_t launch_attn_causal<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                             const AttnArgs&, int, cudaStream_t);
 template cudaError_t launch_attn_causal<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,

@@ -57,6 +57,18 @@ struct AttnArgs {
     float in_inv_Sl;  // 1 / in_Sl (fp32), for a division-free shard lookup
 };
 
+// Packed variable-length sequences (B = 1, S = T rows in total): the sequence
+// boundaries and the list of query tiles, built on the host and passed by value
+// in the launch's parameter space (about 20 KB), so a call needs no device memory.
+constexpr int MAX_VARLEN_SEQS = 1024;
+constexpr int MAX_VARLEN_TILES = 4096;
+struct VarlenTable {
+    int n_seqs;
+    int n_tiles;                          // entries of `tile` (units = n_tiles * H)
+    int cu[MAX_VARLEN_SEQS + 1];          // packed row of each sequence start; cu[n_seqs] = T
+    unsigned tile[MAX_VARLEN_TILES];      // (sequence << 16) | query tile, longest first
+};
+
 // Tensor maps of Q, K, V given as P sequence shards [B, S/P, H, D] each (the
 // layout every Ulysses rank holds before the pre-attention All-to-All).
 struct ShardMaps {
@@ -79,6 +91,13 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 template <int D>
 cudaError_t launch_attn_causal(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const AttnArgs& args, int grid, cudaStream_t stream);
+
+// Packed variable-length sequences (causal or not): tiles of vt run whole in the
+// listed order; args.B = 1, args.S = T, args.units = vt.n_tiles * H.
+template <int D>
+cudaError_t launch_attn_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const AttnArgs& args, const VarlenTable& vt, bool causal, int grid,
+                               cudaStream_t stream);
 
 // The same kernel reading Q, K, V from P sequence shards (args.in_Sl = S / P).
 template <int D>

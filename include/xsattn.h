@@ -281,6 +281,41 @@ int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, 
                        int B, int S, int H, int D, int P, float scale, void* stream);
 
 /*
+ * xs_attn_varlen_fwd -- attention over packed variable-length sequences with the
+ * same fused output layouts.  The X-Stage pages batch equal-length DiT
+ * sequences and define no packed form; this is the usual variable-length batch:
+ * n_seqs sequences of lengths seqlens[0..n_seqs) lie back to back along the
+ * rows of one [T, H, D] tensor per operand (T = their sum; sequence i holds rows
+ * [c_i, c_i + seqlens[i]), c_i = seqlens[0] + ... + seqlens[i-1]), and row s of
+ * sequence i attends only to that sequence's keys:
+ *     O[s,h,:] = sum_t exp(x_t - m) V[t,h,:] / sum_t exp(x_t - m),
+ *     t over [c_i, c_i + seqlens[i])  (causal != 0: over [c_i, s]).
+ *   q, k, v   device bf16 [T, H, D] (16-byte aligned), read only.
+ *   seqlens   HOST int array of n_seqs lengths, each >= 0 (empty sequences are
+ *             skipped), read before the call returns.
+ *   n_seqs    1 .. 1024.
+ *   causal    0: attend to the whole sequence; otherwise causal within it.
+ *   layout    XS_LAYOUT_A2A: outs = P sequence shards [T/P, H, D] of the packed
+ *             rows (shard p holds rows [p*T/P, (p+1)*T/P), whichever sequences
+ *             they belong to; T % P == 0 and H % P == 0);
+ *             XS_LAYOUT_CONTIGUOUS: outs[0] = [T, H, D] (P ignored);
+ *             XS_LAYOUT_HEADS: outs = P head shards [T, H/P, D].
+ * Limits: at most 4096 query tiles of 128 rows in all (sum of ceil(len/128));
+ * a sequence at most 8,388,608 rows.  The library builds the tile list on the
+ * host (longest first) and passes it in the launch's parameter space (about
+ * 20 KB): the call allocates no device memory.  With equal lengths the result is
+ * bit-identical to xs_attn_a2a_fwd / xs_attn_causal_fwd on the [B, S, H, D] view
+ * of the same memory.
+ * Returns XS_OK; XS_ERR_NULL (q, k, v, outs, an out pointer or seqlens);
+ * XS_ERR_SHAPE (n_seqs out of range, a negative or too long length, lengths not
+ * summing to T, too many tiles, H < 1); the checks of xs_attn_a2a_fwd otherwise
+ * (with B = 1, S = T); asynchronous on `stream`.
+ */
+int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* seqlens, int n_seqs,
+                       int causal, int layout, void* const* outs, int T, int H, int D, int P, float scale,
+                       void* stream);
+
+/*
  * xs_burst_gap -- Burst-Gap microbenchmark of the store path the fused epilogue
  * uses (SM -> L2 -> HBM on one GPU).  X-Stage (arXiv 2607.23264), gist.science
  * technical summary, "Methodology: The X-Stage Abstraction and Burst-Gap

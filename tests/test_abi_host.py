@@ -172,6 +172,34 @@ def test_causal_validation(xs):
         xs.XS_ERR_OVERLAP
 
 
+def test_varlen_validation(xs):
+    lib = xs.lib
+    outs = _outs(2)
+    A2A, CONT = xs.XS_LAYOUT_A2A, xs.XS_LAYOUT_CONTIGUOUS
+
+    def call(lens, T=None, causal=0, layout=A2A, o=outs, H=2, D=64, P=2, q=Q, scale=0.1):
+        arr = (ctypes.c_int * max(1, len(lens)))(*lens)
+        T = sum(lens) if T is None else T
+        return lib.xs_attn_varlen_fwd(q, K, V, arr, len(lens), causal, layout, o, T, H, D, P, scale, None)
+
+    assert lib.xs_attn_varlen_fwd(Q, K, V, None, 1, 0, A2A, outs, 256, 2, 64, 2, 0.1, None) == xs.XS_ERR_NULL
+    assert call([256], o=None) == xs.XS_ERR_NULL
+    assert call([]) == xs.XS_ERR_SHAPE                          # no sequence
+    assert call([1] * 1025, T=1026) == xs.XS_ERR_SHAPE          # too many sequences
+    assert call([300, -44]) == xs.XS_ERR_SHAPE                  # negative length
+    assert call([100, 156], T=250) == xs.XS_ERR_SHAPE           # lengths do not sum to T
+    assert call([4097 * 128], layout=CONT, P=1) == xs.XS_ERR_SHAPE       # 4097 tiles
+    assert call([8388609], layout=CONT, P=1) == xs.XS_ERR_SHAPE          # sequence too long
+    assert call([0, 0]) == xs.XS_ERR_SHAPE                      # T = 0
+    assert call([100, 156], layout=9) == xs.XS_ERR_LAYOUT
+    assert call([100, 155]) == xs.XS_ERR_DIVISIBILITY           # T % P != 0 for the A2A shards
+    assert call([100, 156], H=3) == xs.XS_ERR_DIVISIBILITY
+    assert call([100, 156], D=96) == xs.XS_ERR_HEAD_DIM
+    assert call([100, 156], q=Q + 8) == xs.XS_ERR_ALIGNMENT
+    assert call([100, 156], scale=-1.0) == xs.XS_ERR_SCALE
+    assert call([100, 156], layout=CONT, P=1, o=_outs(1, base=K + 64)) == xs.XS_ERR_OVERLAP
+
+
 def test_workspace_query_validation(xs):
     import ctypes
     lib = xs.lib
