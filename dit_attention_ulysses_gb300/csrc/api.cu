@@ -504,7 +504,9 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
     if ((rc = device_info(&dev)) != XS_OK) return rc;
 
     // The tile list, longest first: tile (i, t) reads ceil(len_i / 128) key blocks,
-    // or t + 1 when causal; ties keep sequence order, then query-tile order.
+    // or t + 1 when causal; ties keep sequence order, then query-tile order (the
+    // sort is stable), so without the mask a sequence's tiles stay together, tile 0
+    // first, which the kernel's head-major order within a sequence relies on.
     static thread_local xs::VarlenTable vt;   // 20 KB: kept off the stack
     vt.n_seqs = n_seqs;
     vt.cu[0] = 0;

@@ -215,9 +215,13 @@ __device__ __forceinline__ long long sk_start(const AttnArgs& a, int i) {
 // tile index grows with idx.
 //
 // VARLEN: packed sequences (B = 1, S = their total length).  vt->tile lists the
-// query tiles (sequence, query tile) longest first; unit u is entry u / H of it
-// for head u % H, dealt out in the same snake order.  A tile of sequence i
-// reads the key blocks of that sequence only: ceil(len_i / 128) of them, or
+// query tiles (sequence, query tile) longest first, dealt out in the same snake
+// order.  CAUSAL: unit u is entry u / H for head u % H.  Otherwise every tile of
+// a sequence has the same length, the list holds a sequence's tiles together
+// (query tile 0 first), and the sequence's units [H * first, H * (first + nq))
+// run head-major, the query tiles of one head side by side, so that the CTAs
+// working at once share that head's keys and values in L2.  A tile of sequence
+// i reads the key blocks of that sequence only: ceil(len_i / 128) of them, or
 // (CAUSAL) qt + 1.
 template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* vt, int idx, Work& w) {
@@ -227,13 +231,21 @@ __device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* v
         const long long u = static_cast<long long>(idx) * G + ((idx & 1) ? G - 1 - i : i);
         if (u >= a.units) return false;
         const int t = static_cast<int>(u) / a.H;
-        w.h = static_cast<int>(u) - t * a.H;
         const unsigned e = vt->tile[t];
         const int seq = static_cast<int>(e >> 16);
-        w.qt = static_cast<int>(e & 0xffffu);
         w.b = 0;
         w.row0 = vt->cu[seq];
         w.len = vt->cu[seq + 1] - w.row0;
+        if constexpr (CAUSAL) {
+            w.h = static_cast<int>(u) - t * a.H;
+            w.qt = static_cast<int>(e & 0xffffu);
+        } else {
+            const int nq = (w.len + BLOCK_M - 1) / BLOCK_M;
+            const int first = t - static_cast<int>(e & 0xffffu);   // list index of the sequence's tile 0
+            const int v = static_cast<int>(u) - first * a.H;      // unit within the sequence, < nq * H
+            w.h = v / nq;
+            w.qt = v - w.h * nq;
+        }
         w.k0 = 0;
         w.nb = CAUSAL ? w.qt + 1 : (w.len + BLOCK_N - 1) / BLOCK_N;
         w.kind = WORK_FULL;
