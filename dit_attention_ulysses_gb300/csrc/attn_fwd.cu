@@ -212,7 +212,10 @@ __device__ __forceinline__ long long sk_start(const AttnArgs& a, int i) {
 // CTA in snake order: CTAs 0 .. G-1 in even waves, G-1 .. 0 in odd ones, so
 // that the CTA given the longest tile of a wave gets the shortest of the next.
 // The sequence of a CTA ends at the first index past the last tile, since the
-// tile index grows with idx.
+// tile index grows with idx.  With a.causal_head_major the tiles go head by
+// head instead (query tiles descending within a head): concurrent CTAs then
+// share one head's keys and values in L2, at some cost in balance, which the
+// host accepts only where it is small (long sequences).
 //
 // VARLEN: packed sequences (B = 1, S = their total length).  vt->tile lists the
 // query tiles (sequence, query tile) longest first, dealt out in the same snake
@@ -255,10 +258,16 @@ __device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* v
     if constexpr (CAUSAL) {
         const long long u = static_cast<long long>(idx) * G + ((idx & 1) ? G - 1 - i : i);
         if (u >= a.units) return false;
-        const int bhs = a.B * a.H;
         const int t = static_cast<int>(u);
-        const int bh = t % bhs;
-        w.qt = a.n_qt - 1 - t / bhs;
+        int bh;
+        if (a.causal_head_major) {
+            bh = t / a.n_qt;
+            w.qt = a.n_qt - 1 - (t - bh * a.n_qt);
+        } else {
+            const int bhs = a.B * a.H;
+            bh = t % bhs;
+            w.qt = a.n_qt - 1 - t / bhs;
+        }
         w.h = bh % a.H;
         w.b = bh / a.H;
         w.k0 = 0;

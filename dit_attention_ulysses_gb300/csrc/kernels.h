@@ -55,6 +55,9 @@ struct AttnArgs {
     int in_Sl;      // inputs as sequence shards: rows per shard (a multiple of 128);
                     // 0: one [B, S, H, D] tensor per operand
     float in_inv_Sl;  // 1 / in_Sl (fp32), for a division-free shard lookup
+    int causal_head_major;  // causal tile order: 0 longest first with the B*H tiles of one
+                            // query tile side by side; 1 head-major (a head's query tiles
+                            // side by side, longest first within the head)
 };
 
 // Packed variable-length sequences (B = 1, S = T rows in total): the sequence

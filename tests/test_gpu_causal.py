@@ -1,6 +1,8 @@
 """GPU parity of causal attention (xs_attn_causal_fwd): query row s attends to
-keys 0 .. s.  Tiles read key blocks 0 .. t only (t = the query tile), the
-diagonal block is masked per row, and tiles are scheduled longest first.
+keys 0 .. s.  Tiles read key blocks 0 .. t only (t = the query tile) and the
+diagonal block is masked per row.  Tiles run in one of two orders chosen on the
+host (longest first with the heads side by side, or head-major where that
+balances as well); both are exercised.
 
 Checked against the fp64 oracle's causal entries (element by element at
 sizes the oracle finishes in seconds, spanning several tiles, more than one
@@ -143,11 +145,15 @@ def test_causal_last_row_equals_bidirectional(xs, S):
     assert not torch.equal(causal[:, 0].view(torch.int16), full[:, 0].view(torch.int16))
 
 
-@pytest.mark.parametrize("B,S,H,D,P", [(1, 4608, 24, 128, 4), (1, 4000, 5, 128, 5), (2, 512, 4, 64, 2)])
+@pytest.mark.parametrize("B,S,H,D,P", [(1, 4608, 24, 128, 4), (1, 4000, 5, 128, 5), (2, 512, 4, 64, 2),
+                                       (1, 75776, 40, 128, 8)],
+                         ids=["image", "ragged_two_waves", "d64", "video_large"])
 def test_causal_layout_code_bit_exact(xs, B, S, H, D, P):
     """Index-coded inputs: the own key dominates every other by a weight ratio
     below fp32 resolution and lies inside the causal window, so every output
-    row is its own V row exactly, in the owning shard at the right head."""
+    row is its own V row exactly, in the owning shard at the right head.  The
+    image shape runs the longest-first tile order, the others the head-major
+    one (the large video-DiT shape at full size)."""
     q, k, v, scale = di.layout_code_inputs_torch(B, S, H, D)
     outs = _causal(xs, q, k, v, P, scale)
     Sl = S // P
