@@ -14,6 +14,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <vector>
 
@@ -254,9 +255,9 @@ unsigned next_epoch() {
 // (measured: ~3 us per tile against ~0.9 us per block).  Longest first with the
 // B*H tiles of one query tile side by side balances best; head-major keeps the
 // concurrent CTAs on one head's keys and values in L2.  Head-major is taken when
-// its modelled makespan is within 2 % of longest-first's.
-bool causal_head_major(int BH, int n_qt, int grid) {
-    if (grid < 1) return false;
+// its modelled makespan is within 2 % of longest-first's.  The model walks every
+// tile once, so its answer is kept per (B*H, tiles per head, grid).
+bool causal_order_model(int BH, int n_qt, int grid) {
     std::vector<double> lpt(grid, 0.0), hm(grid, 0.0);
     const long long units = static_cast<long long>(BH) * n_qt;
     for (long long u = 0; u < units; ++u) {
@@ -267,6 +268,30 @@ bool causal_head_major(int BH, int n_qt, int grid) {
     }
     const double a = *std::max_element(lpt.begin(), lpt.end()), b = *std::max_element(hm.begin(), hm.end());
     return b <= 1.02 * a;
+}
+
+struct OrderKey {
+    int bh, n_qt, grid;
+    bool operator<(const OrderKey& o) const {
+        return bh != o.bh ? bh < o.bh : n_qt != o.n_qt ? n_qt < o.n_qt : grid < o.grid;
+    }
+};
+std::mutex g_order_mutex;
+std::map<OrderKey, bool> g_order_cache;
+
+bool causal_head_major(int BH, int n_qt, int grid) {
+    if (grid < 1) return false;
+    const OrderKey key{BH, n_qt, grid};
+    {
+        std::lock_guard<std::mutex> lock(g_order_mutex);
+        auto it = g_order_cache.find(key);
+        if (it != g_order_cache.end()) return it->second;
+    }
+    const bool hm = causal_order_model(BH, n_qt, grid);
+    std::lock_guard<std::mutex> lock(g_order_mutex);
+    if (g_order_cache.size() >= 256) g_order_cache.clear();
+    g_order_cache[key] = hm;
+    return hm;
 }
 
 // causal: row s attends to keys 0 .. s (one tensor per operand, plain schedule
@@ -513,6 +538,7 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
         tiles += (seqlens[i] + 127) / 128;
     }
     if (total != T || tiles > xs::MAX_VARLEN_TILES) return XS_ERR_SHAPE;
+    if (tiles * static_cast<int64_t>(H) > INT32_MAX) return XS_ERR_SHAPE;   // units must fit an int
     xs::EpiParams epi;
     int n_out = 0;
     int64_t out_bytes = 0;

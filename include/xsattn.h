@@ -301,14 +301,14 @@ int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, 
  *             XS_LAYOUT_CONTIGUOUS: outs[0] = [T, H, D] (P ignored);
  *             XS_LAYOUT_HEADS: outs = P head shards [T, H/P, D].
  * Limits: at most 4096 query tiles of 128 rows in all (sum of ceil(len/128));
- * a sequence at most 8,388,608 rows.  The library builds the tile list on the
+ * a sequence at most 8,388,608 rows; tiles x H at most 2^31 - 1.  The library builds the tile list on the
  * host (longest first) and passes it in the launch's parameter space (about
  * 20 KB): the call allocates no device memory.  With equal lengths the result is
  * bit-identical to xs_attn_a2a_fwd / xs_attn_causal_fwd on the [B, S, H, D] view
  * of the same memory.
  * Returns XS_OK; XS_ERR_NULL (q, k, v, outs, an out pointer or seqlens);
  * XS_ERR_SHAPE (n_seqs out of range, a negative or too long length, lengths not
- * summing to T, too many tiles, H < 1); the checks of xs_attn_a2a_fwd otherwise
+ * summing to T, too many tiles or tiles x H, H < 1); the checks of xs_attn_a2a_fwd otherwise
  * (with B = 1, S = T); asynchronous on `stream`.
  */
 int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* seqlens, int n_seqs,

@@ -198,6 +198,9 @@ def test_varlen_validation(xs):
     assert call([100, 156], q=Q + 8) == xs.XS_ERR_ALIGNMENT
     assert call([100, 156], scale=-1.0) == xs.XS_ERR_SCALE
     assert call([100, 156], layout=CONT, P=1, o=_outs(1, base=K + 64)) == xs.XS_ERR_OVERLAP
+    # 1024 one-row sequences are 1024 tiles; with 2**21 + 1 heads the work units
+    # (tiles x heads) would overflow an int although the dense-shape limits hold
+    assert call([1] * 1024, layout=CONT, P=1, H=2 ** 21 + 1, D=64) == xs.XS_ERR_SHAPE
 
 
 def test_workspace_query_validation(xs):
