@@ -14,9 +14,11 @@
  * global head index.
  *
  * Layout conventions (all entry points):
- *   - bf16 tensors, row-major [B, S, H, D] with D fastest ("BSHD"), contiguous.
+ *   - bf16 tensors, row-major [B, S, H, D] with D fastest ("BSHD"), contiguous
+ *     (xs_attn_varlen_fwd: packed [T, H, D]).
  *   - Attention is bidirectional (non-causal): O = softmax(Q K^T * scale) V per
- *     (b, h), no mask, no bias, no dropout.  Accumulation is fp32, the
+ *     (b, h), no mask, no bias, no dropout, except in xs_attn_causal_fwd and,
+ *     when asked, xs_attn_varlen_fwd.  Accumulation is fp32, the
  *     probabilities are rounded to bf16 before the PV product, the output is
  *     rounded to bf16 (round to nearest even).
  *   - D must be 64 or 128.  S, B, H >= 1; S need not be a multiple of the tile.
@@ -24,7 +26,8 @@
  *
  * Ownership and synchronisation:
  *   - The caller owns every buffer and the stream.  The library allocates no
- *     device memory per call; it keeps one device error word per process.
+ *     device memory per call; on each device it keeps one error word and the
+ *     scratch array of xs_attn_fwd_balanced_noalloc (static device data).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  Outputs are valid once the stream reaches the end of
  *     the call.  Inputs are never modified.
