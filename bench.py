@@ -230,6 +230,17 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def varlen_mix(total: int, seed: int = 12345):
+    """Sequence lengths covering `total` tokens: drawn uniformly in [total/16, total/2)
+    from a seeded generator until they cover it, the last one cut to fit."""
+    rng = np.random.default_rng(seed)
+    lens = []
+    while sum(lens) < total:
+        lens.append(int(rng.integers(max(1, total // 16), max(2, total // 2))))
+    lens[-1] -= sum(lens) - total
+    return lens
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -292,14 +303,9 @@ def run_ours(args, rank, world, local_rank):
     def causal():
         xs.xs_attn_causal_fwd(q, k, v, xs.XS_LAYOUT_A2A, causal_out, w.scale, stream)
 
-    # packed variable-length sequences: the same B*S tokens as a seeded mix of lengths
-    # between (B*S)/16 and (B*S)/2 (the last one cut to fit), bidirectional within each
+    # packed variable-length sequences: the same B*S tokens, bidirectional within each
     T = B * S
-    rng = np.random.default_rng(12345)
-    seqlens = []
-    while sum(seqlens) < T:
-        seqlens.append(int(rng.integers(max(1, T // 16), max(2, T // 2))))
-    seqlens[-1] -= sum(seqlens) - T
+    seqlens = varlen_mix(T)
     q_p, k_p, v_p = (x.view(T, H, D) for x in (q, k, v))
     varlen_out = [torch.empty((T // P, H, D), dtype=torch.bfloat16, device=dev) for _ in range(P)]
 

@@ -75,3 +75,18 @@ def test_reference_arm_runs_oracle_on_cpu():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["unit"] == "TFLOP/s"
+
+
+def test_varlen_mix_covers_the_tokens_within_the_table_limits():
+    """The bench's packed-sequence line regroups each workload's B*S tokens; the mix
+    must cover them exactly with positive lengths and fit the library's table
+    (1024 sequences, 4096 tiles of 128 rows)."""
+    import bench
+    import dit_inputs as di
+    for w in di.WORKLOADS.values():
+        T = w.B * w.S
+        lens = bench.varlen_mix(T)
+        assert sum(lens) == T and min(lens) >= 1, w.name
+        assert len(lens) <= 1024 and sum((n + 127) // 128 for n in lens) <= 4096, w.name
+        assert lens == bench.varlen_mix(T)   # seeded: the same mix every run
+    assert bench.varlen_mix(4608) == [1697, 746, 1877, 288]
