@@ -110,10 +110,14 @@ def test_varlen_layouts_bit_identical(xs, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_varlen_layout_code_bit_exact(xs, causal):
+@pytest.mark.parametrize("seqlens,H,D,P", [([1000, 1, 129, 0, 918], 8, 128, 4),
+                                           ([27916, 12272, 30881, 4707], 40, 128, 8)],
+                         ids=["mix", "video_large_tokens"])
+def test_varlen_layout_code_bit_exact(xs, seqlens, H, D, P, causal):
     """Index-coded inputs over the packed rows: each row's own key dominates
-    every other key of its sequence, so every output row is its own V row."""
-    seqlens, H, D, P = [1000, 1, 129, 0, 918], 8, 128, 4
+    every other key of its sequence, so every output row is its own V row.  The
+    second case packs the large video-DiT shape's 75776 tokens as the bench's
+    seeded mix of four sequences."""
     T = sum(seqlens)
     q, k, v, scale = di.layout_code_inputs_torch(1, T, H, D)
     outs = _run(xs, q[0], k[0], v[0], seqlens, xs.XS_LAYOUT_A2A, P, scale, causal)
