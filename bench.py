@@ -230,6 +230,12 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def step_percentiles(ms):
+    """p10, p50 and p90 of per-step times (ms), for any number of steps >= 1."""
+    p10, p50, p90 = np.percentile(np.asarray(ms, dtype=np.float64), [10, 50, 90])
+    return {"p10": float(p10), "p50": float(p50), "p90": float(p90)}
+
+
 def varlen_mix(total: int, seed: int = 12345):
     """Sequence lengths covering `total` tokens: drawn uniformly in [total/16, total/2)
     from a seeded generator until they cover it, the last one cut to fit."""
@@ -401,6 +407,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
+        "step_ms_percentiles": step_percentiles(per_step),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,

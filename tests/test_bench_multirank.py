@@ -90,3 +90,11 @@ def test_varlen_mix_covers_the_tokens_within_the_table_limits():
         assert len(lens) <= 1024 and sum((n + 127) // 128 for n in lens) <= 4096, w.name
         assert lens == bench.varlen_mix(T)   # seeded: the same mix every run
     assert bench.varlen_mix(4608) == [1697, 746, 1877, 288]
+
+
+def test_step_percentiles():
+    """p10/p50/p90 of the timed steps (linear interpolation), also for one step."""
+    import bench
+    assert bench.step_percentiles([2.5]) == {"p10": 2.5, "p50": 2.5, "p90": 2.5}
+    got = bench.step_percentiles([float(x) for x in range(10, 0, -1)])   # order does not matter
+    assert abs(got["p10"] - 1.9) < 1e-12 and abs(got["p50"] - 5.5) < 1e-12 and abs(got["p90"] - 9.1) < 1e-12
