@@ -5,7 +5,7 @@ output tile stored into its owner's sequence shard) on one batch of seeded
 synthetic bf16 input already resident in HBM.  Metric: TFLOP/s of the
 4*B*H*S^2*D tensor FLOPs, whole-job (summed over ranks).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload image]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload video_large]
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
 
 Prints ONE JSON line (rank 0).  Between timed steps the L2 cache is flushed by
@@ -32,11 +32,12 @@ import numpy as np  # noqa: E402
 
 import dit_inputs as di  # noqa: E402
 
-DEFAULT_WORKLOAD = "image"
+DEFAULT_WORKLOAD = "video_large"
+SIDE_WORKLOAD = "image"   # timed as an extra key of the default line
 METRIC = "fused attn+A2A-layout TFLOP/s and % of GB300 dense BF16 peak; fused-store overhead %"
 KERNEL_SOURCES = ["dit_attention_ulysses_gb300/csrc/attn_fwd.cu", "dit_attention_ulysses_gb300/csrc/ptx.cuh",
                   "dit_attention_ulysses_gb300/csrc/kernels.h"]
-NCU_SUMMARY = os.path.join(ROOT, "profiles", "ncu_attn_a2a_kernel_image.txt")
+PROFILES = os.path.join(ROOT, "profiles")
 
 
 def env_rank():
@@ -60,23 +61,44 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
-    if it was taken on this workload and on the current kernel source."""
-    if not os.path.exists(NCU_SUMMARY):
-        return None
+def _read_summary(path):
     vals = {}
-    with open(NCU_SUMMARY) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash() or vals.get("workload") != workload:
-        return None
-    try:
-        return int(float(vals["dram_bytes_per_launch_full_workload"]))
-    except (KeyError, ValueError):
-        return None
+    return vals
+
+
+def tiles_of(w) -> int:
+    return w.B * w.H * ((w.S + 127) // 128)
+
+
+def ncu_traffic(w):
+    """DRAM bytes per launch of the fused kernel from a committed ncu summary taken on
+    the current kernel source: the workload's own capture, else a capture of a smaller
+    workload scaled by query tiles (K/V of the head being worked on stay in L2, so every
+    tile moves the same bytes: its Q and O tiles and its share of the head's K and V).
+    Returns (bytes or None, note)."""
+    names = sorted(f for f in os.listdir(PROFILES) if f.startswith("ncu_attn_a2a_kernel_") and f.endswith(".txt"))
+    own = f"ncu_attn_a2a_kernel_{w.name}.txt"
+    if own in names:
+        names.remove(own)
+        names.insert(0, own)
+    for name in names:
+        vals = _read_summary(os.path.join(PROFILES, name))
+        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+            continue
+        try:
+            if vals.get("workload") == w.name:
+                return int(float(vals["dram_bytes_per_launch_full_workload"])), f"ncu capture of {w.name} ({name})"
+            per_tile = float(vals["dram_bytes_per_tile"])
+        except (KeyError, ValueError):
+            continue
+        return int(per_tile * tiles_of(w)), (f"ncu capture of {vals.get('workload')} ({name}), "
+                                             f"{per_tile:.0f} B per query tile x {tiles_of(w)} tiles")
+    return None, "no ncu capture of the current kernel source"
 
 
 class ClockSampler:
@@ -165,10 +187,11 @@ def time_steps(torch, fn, steps, flush, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def cpu_oracle_sample(w, seconds_target=12.0, max_rows=None):
-    """Time the fp64 oracle on a bounded sample of query rows (all heads) of workload w."""
+def cpu_oracle_sample(w, seconds_target=12.0, max_rows=None, inputs=None):
+    """Time the fp64 oracle on a bounded sample of query rows (all heads) of workload w.
+    Returns the cpu_baseline object and (rows_b, rows_s, oracle rows [n, H, D])."""
     import oracle
-    q, k, v = di.random_qkv(w)
+    q, k, v = di.random_qkv(w) if inputs is None else inputs
     threads = oracle.threads_used()
     per_pair = 4.0 * w.S * w.D  # flops per (row, head)
     # calibrate on a sample large enough to occupy every thread for a while
@@ -187,12 +210,25 @@ def cpu_oracle_sample(w, seconds_target=12.0, max_rows=None):
     n = max(8, min(n, w.B * w.S if max_rows is None else max_rows))
     rb, rs = di.sample_rows(w, n, seed=6)
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.scale, rb, rs)
+    ref = oracle.attention_rows(q, k, v, w.scale, rb, rs)
     dt = time.perf_counter() - t0
     flops = len(rb) * w.H * per_pair
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+    line = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(rb)} query rows x {w.H} heads of the {w.name} workload ({flops:.3e} FLOPs, "
                       f"{dt:.1f} s, fp64 C/OpenMP)"}
+    return line, (rb, rs, ref)
+
+
+def sampled_parity(w, outs, rb, rs, ref):
+    """The fused output at the oracle's sampled rows against the oracle: max-abs error,
+    relative L2 error and how many elements exceed the flat 2e-2 bar."""
+    Sl = w.S // w.P
+    got = np.stack([outs[int(s) // Sl][int(b), int(s) % Sl].float().cpu().numpy() for b, s in zip(rb, rs)])
+    err = np.abs(got.astype(np.float64) - ref)
+    return {"rows": int(len(rb)), "elements": int(err.size), "max_abs": float(err.max()),
+            "rel_l2": float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)),
+            "n_above_2e-2": int((err > 2e-2).sum()), "max_abs_ref": float(np.abs(ref).max()),
+            "against": "fp64 oracle rows of the cpu_baseline sample (all heads)"}
 
 
 def run_reference(args, rank, world):
@@ -245,6 +281,25 @@ def varlen_mix(total: int, seed: int = 12345):
         lens.append(int(rng.integers(max(1, total // 16), max(2, total // 2))))
     lens[-1] -= sum(lens) - total
     return lens
+
+
+def side_workload_line(torch, xs, args, dev, stream, flush):
+    """The fused call on the image-DiT workload, timed like the main line (L2 flushed
+    before each step), reported beside it."""
+    w = di.WORKLOADS[SIDE_WORKLOAD]
+    q, k, v = (to_device(x, torch, dev) for x in di.random_qkv(w))
+    outs = [torch.empty((w.B, w.S // w.P, w.H, w.D), dtype=torch.bfloat16, device=dev) for _ in range(w.P)]
+    ws = xs.Workspace.for_shape(w.B, w.S, w.H, w.D, device=dev) if args.schedule == "balanced" else None
+    fn = lambda: xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_A2A, outs, w.scale, ws, stream)
+    for _ in range(3):
+        fn()
+    n = max(10, min(args.steps, 50))
+    ms = time_steps(torch, fn, n, flush, stream)
+    if xs.xs_attn_get_device_error(stream) != 0:
+        raise RuntimeError("device error in the side workload")
+    return {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "P": w.P, "steps": n,
+            "ms_per_step": statistics.mean(ms), "tflops": w.flops / (statistics.mean(ms) * 1e-3) / 1e12,
+            "step_ms_percentiles": step_percentiles(ms), "api": "xs_attn_fwd_balanced"}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -394,10 +449,12 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(statistics.mean(time_steps(torch, e2e_fn, n_e2e, flush, stream)), world)
     if xs.xs_attn_get_device_error(stream) != 0:
         raise RuntimeError("device error after ablation / e2e runs")
+    side = side_workload_line(torch, xs, args, dev, stream, flush) if args.workload != SIDE_WORKLOAD else None
 
     if rank != 0:
         return
     peak_tflops, _, peak_kind = measured_peaks()
+    traffic, traffic_note = ncu_traffic(w)
     achieved = w.flops / (statistics.mean(per_step) * 1e-3) / 1e12
     line = {
         "metric": METRIC,
@@ -421,7 +478,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops if peak_tflops else None,
                      "peak_kind": f"{peak_kind} bf16 burst",
-                     "traffic": ncu_traffic(w.name),
+                     "traffic": traffic,
+                     "traffic_source": traffic_note,
                      "algorithmic_bytes": 4 * w.tensor_bytes},
         "overhead_pct": 100.0 * (t_fused - t_alone) / t_alone,
         "ablation": {"attention_alone_ms": t_alone, "fused_ms": t_fused, "attention_plus_relayout_ms": t_serial,
@@ -437,8 +495,12 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),
     }
+    if side is not None:
+        line["side_workload"] = side
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_oracle_sample(w, seconds_target=args.cpu_seconds)
+        line["cpu_baseline"], (rb, rs, ref) = cpu_oracle_sample(w, seconds_target=args.cpu_seconds,
+                                                                inputs=(qb, kb, vb))
+        line["sampled_parity"] = sampled_parity(w, outs, rb, rs, ref)
     line["wall_s_timed_region"] = t_wall1 - t_wall0
     print(json.dumps(line), flush=True)
 

@@ -109,10 +109,16 @@ def test_varlen_layouts_bit_identical(xs, causal):
         assert torch.equal(heads[p].view(torch.int16), full[:, p * Hl:(p + 1) * Hl].view(torch.int16))
 
 
-@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-@pytest.mark.parametrize("seqlens,H,D,P", [([1000, 1, 129, 0, 918], 8, 128, 4),
-                                           ([27916, 12272, 30881, 4707], 40, 128, 8)],
-                         ids=["mix", "video_large_tokens"])
+LAYOUT_CASES = [
+    # seqlens, H, D, P, causal
+    ([1000, 1, 129, 0, 918], 8, 128, 4, False),
+    ([1000, 1, 129, 0, 918], 8, 128, 4, True),
+    ([27916, 12272, 30881, 4707], 40, 128, 8, False),
+]
+
+
+@pytest.mark.parametrize("seqlens,H,D,P,causal", LAYOUT_CASES,
+                         ids=["mix-full", "mix-causal", "video_large_tokens-full"])
 def test_varlen_layout_code_bit_exact(xs, seqlens, H, D, P, causal):
     """Index-coded inputs over the packed rows: each row's own key dominates
     every other key of its sequence, so every output row is its own V row.  The
