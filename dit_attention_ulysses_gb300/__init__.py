@@ -36,6 +36,7 @@ __all__ = [
     "xs_attn_varlen_fwd",
     "Workspace",
     "xs_attn_get_device_error",
+    "xs_attn_get_device_error_info",
     "xs_attn_error_string",
     "attn_a2a",
     "LIB_PATH",
@@ -59,6 +60,9 @@ XS_ERR_DEVICE_TIMEOUT = -10
 XS_ERR_UNSUPPORTED_DEVICE = -11
 XS_ERR_WORKSPACE = -12
 XS_ERR_LAYOUT = -13
+XS_ERR_DEVICE_DRAIN = -14
+XS_ERR_DEVICE_BOUNDS = -15
+XS_ERR_UNAVAILABLE = -16
 XS_MAX_P = 16
 XS_LAYOUT_A2A = 0
 XS_LAYOUT_CONTIGUOUS = 1
@@ -92,6 +96,7 @@ EXPORTS = {
                                        _vp]),
     "xs_burst_gap": (_int, [_vp, _size, _int, _size, _int, ctypes.c_longlong, ctypes.c_longlong, _vp, _vp]),
     "xs_attn_get_device_error": (_int, [_vp]),
+    "xs_attn_get_device_error_info": (_int, [_vp, ctypes.POINTER(_int), _int]),
     "xs_attn_error_string": (ctypes.c_char_p, [_int]),
     "xs_attn_last_cuda_error": (_int, []),
     "xs_attn_version": (_int, []),
@@ -285,6 +290,15 @@ def xs_attn_get_device_error(stream=None) -> int:
     return lib.xs_attn_get_device_error(_stream_handle(stream))
 
 
+def xs_attn_get_device_error_info(stream=None):
+    """Synchronise the stream; return (status code, record of the first device error as a
+    dict) and clear both (see include/xsattn.h for the fields)."""
+    info = (_int * 8)()
+    code = lib.xs_attn_get_device_error_info(_stream_handle(stream), info, 8)
+    keys = ("kind", "cta", "warp", "lane", "site", "detail0", "detail1", "detail2")
+    return code, dict(zip(keys, list(info)))
+
+
 def xs_attn_error_string(code: int) -> str:
     return lib.xs_attn_error_string(code).decode()
 
@@ -323,7 +337,8 @@ def xs_attn_varlen_fwd(q, k, v, seqlens, layout: int, outs, scale: float, causal
                        stream=None) -> None:
     """Attention over packed variable-length sequences: ``q``, ``k``, ``v`` are
     [T, H, D] bf16 holding sequences of lengths ``seqlens`` (host integers) back to
-    back; each row attends to its own sequence (``causal``: up to its own position).
+    back; each row attends to its own sequence.  ``causal=True`` is refused
+    (XsError with XS_ERR_UNAVAILABLE): that form is disabled in this build.
     ``layout`` XS_LAYOUT_A2A (P shards [T/P, H, D]), XS_LAYOUT_CONTIGUOUS (one
     [T, H, D] tensor) or XS_LAYOUT_HEADS (P head shards [T, H/P, D])."""
     T, H, D = _thd(q, "q").shape

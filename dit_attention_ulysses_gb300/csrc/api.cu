@@ -8,8 +8,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <atomic>
-#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -189,7 +187,7 @@ struct Plan {
     int dp_tiles = 0;
     int sk_ctas = 0;
     long long sk_iters = 0;
-    size_t off_ml = 0, off_flag = 0, ws_bytes = 0;   // workspace layout (split only)
+    size_t off_count = 0, off_flag = 0, off_ml = 0, off_o = 0, ws_bytes = 0;   // workspace layout (split only)
 };
 
 constexpr long long MIN_PIECE = 8;    // key blocks per CTA range, at least
@@ -221,28 +219,17 @@ Plan make_plan(int B, int S, int H, int D, const DeviceInfo& dev) {
     pl.sk_iters = sk;
     pl.sk_ctas = static_cast<int>(ctas);
     pl.grid = tiles >= G ? G : pl.sk_ctas;
-    // part_o [grid][128][D] fp32 | part_ml [grid][128] float2 | part_flag [grid][8] u32
+    // launch count [2] u32 | part_flag [SMs][8] u32 | part_ml [grid][128] float2 | part_o [grid][128][D] fp32.
+    // The count and the flags come first, at offsets that depend on the device
+    // only: whatever shapes share a workspace, a flag word only ever holds an
+    // epoch of an earlier launch on it (or zero), never stale partial data.
     const size_t slots = static_cast<size_t>(pl.grid);
-    pl.off_ml = align256(slots * 128 * D * 4);
-    pl.off_flag = pl.off_ml + align256(slots * 128 * 8);
-    pl.ws_bytes = pl.off_flag + align256(slots * 8 * 4);
+    pl.off_count = 0;
+    pl.off_flag = 256;
+    pl.off_ml = pl.off_flag + align256(static_cast<size_t>(G) * 8 * 4);
+    pl.off_o = pl.off_ml + align256(slots * 128 * 8);
+    pl.ws_bytes = pl.off_o + align256(slots * 128 * D * 4);
     return pl;
-}
-
-// Launch epochs mark the flags of split tiles.  They start at a per-process
-// value taken from the clock (so that flags left in a reused workspace by
-// another process are unlikely to match) and skip 0.
-std::atomic<unsigned> g_epoch{0};
-std::once_flag g_epoch_once;
-
-unsigned next_epoch() {
-    std::call_once(g_epoch_once, [] {
-        const auto t = std::chrono::high_resolution_clock::now().time_since_epoch().count();
-        g_epoch.store(static_cast<unsigned>(t ^ (t >> 32)) | 1u);
-    });
-    unsigned e = g_epoch.fetch_add(1) + 1;
-    if (e == 0) e = g_epoch.fetch_add(1) + 1;
-    return e;
 }
 
 // ws == nullptr: plain schedule.  Otherwise the balanced schedule whenever it
@@ -322,10 +309,10 @@ int run_attention(const void* q, const void* k, const void* v, const void* const
         a.sp.dp_tiles = pl.dp_tiles;
         a.sp.sk_iters = pl.sk_iters;
         a.sp.sk_ctas = pl.sk_ctas;
-        a.sp.part_o = reinterpret_cast<float*>(base);
+        a.sp.part_o = reinterpret_cast<float*>(base + pl.off_o);
         a.sp.part_ml = reinterpret_cast<float2*>(base + pl.off_ml);
         a.sp.part_flag = reinterpret_cast<unsigned*>(base + pl.off_flag);
-        a.sp.epoch = next_epoch();
+        a.sp.launch_count = reinterpret_cast<unsigned*>(base + pl.off_count);
     } else {
         a.sp.dp_tiles = a.units;
         grid = a.units < dev.sms ? a.units : dev.sms;
@@ -430,7 +417,8 @@ int attn_layout_call(const void* q, const void* k, const void* v, int layout, vo
 // cudaMalloc can fail there, and cudaFree synchronises the whole device) get the
 // balanced schedule's workspace from this file-scope array instead of from a
 // buffer of their own.  It is zero-filled when the module is loaded, which is
-// all the split-tile flags need (a zero flag never matches a launch epoch).
+// all the split-tile flags and the launch count need (a zero flag never matches
+// a launch epoch).
 // 11 MiB covers the largest workspace the schedule asks for on a 152-SM GB300
 // (D = 128: 152 slots x 66,592 B ~ 10.1 MB); a larger need is refused with
 // XS_ERR_WORKSPACE.
@@ -438,21 +426,63 @@ constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(11) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_scratch_mutex;
-void* g_scratch_addr[MAX_DEVICES] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id = 0;   // unique id of the context the address belongs to (0: none yet)
+    void* addr = nullptr;
+};
+ScratchAddr g_scratch_addr[MAX_DEVICES];
 
-// Address of this device's copy of g_noalloc_scratch, looked up once per device.
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
+using PFN_ctxGetId = CUresult (*)(CUcontext, unsigned long long*);
+PFN_ctxGetCurrent g_ctx_get_current = nullptr;
+PFN_ctxGetId g_ctx_get_id = nullptr;
+std::once_flag g_ctx_fn_once;
+
+// Unique id of the calling thread's current context (cuCtxGetId: never reused
+// within the process, unlike the context handle), 0 when there is none.
+int current_context_id(unsigned long long* id) {
+    std::call_once(g_ctx_fn_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<PFN_ctxGetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<PFN_ctxGetId>(p);
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return cuda_fail(cudaErrorSymbolNotFound);
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return cuda_fail(cudaErrorDeviceUninitialized);
+    *id = 0;
+    if (ctx && g_ctx_get_id(ctx, id) != CUDA_SUCCESS) return cuda_fail(cudaErrorDeviceUninitialized);
+    return XS_OK;
+}
+
+// Address of g_noalloc_scratch in the current device's context.  It is looked
+// up (cudaGetSymbolAddress, which also loads the module into the context if
+// needed) the first time a device is used and again whenever the device's
+// current context is a different one than at the last lookup (after
+// cudaDeviceReset, say, the module is loaded anew and the array may move).
 int noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= MAX_DEVICES) return XS_ERR_UNSUPPORTED_DEVICE;
+    unsigned long long id = 0;
+    int rc = current_context_id(&id);
+    if (rc != XS_OK) return rc;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr& s = g_scratch_addr[dev];
+    if (id == 0 || s.ctx_id != id || !s.addr) {
         void* p = nullptr;
         if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
-        g_scratch_addr[dev] = p;
+        if ((rc = current_context_id(&id)) != XS_OK) return rc;   // the lookup made the context current
+        s.ctx_id = id;
+        s.addr = p;
     }
-    *out = g_scratch_addr[dev];
+    *out = s.addr;
     return XS_OK;
 }
 
@@ -539,6 +569,9 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
     }
     if (total != T || tiles > xs::MAX_VARLEN_TILES) return XS_ERR_SHAPE;
     if (tiles * static_cast<int64_t>(H) > INT32_MAX) return XS_ERR_SHAPE;   // units must fit an int
+    // The causal form is not launched: at 75,776 packed tokens its kernel ended
+    // in an unspecified launch failure whose cause is not established.
+    if (causal) return XS_ERR_UNAVAILABLE;
     xs::EpiParams epi;
     int n_out = 0;
     int64_t out_bytes = 0;
@@ -771,13 +804,21 @@ int xs_burst_gap(void* dst, size_t dst_bytes, int producers, size_t burst_bytes,
     return XS_OK;
 }
 
-int xs_attn_get_device_error(void* stream) {
+int xs_attn_get_device_error_info(void* stream, int* info, int n_info) {
+    if (n_info < 0 || n_info > 8 || (n_info > 0 && !info)) return XS_ERR_NULL;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
-    int v = 0;
-    if ((e = xs::read_and_clear_device_error(&v)) != cudaSuccess) return cuda_fail(e);
-    return v == 0 ? XS_OK : XS_ERR_DEVICE_TIMEOUT;
+    int v = 0, drain = 0;
+    xs::DeviceErrorInfo r{};
+    if ((e = xs::read_and_clear_device_error(&v, &r, &drain)) != cudaSuccess) return cuda_fail(e);
+    const int fields[8] = {v ? r.code : 0, r.cta, r.warp, r.lane, r.site, r.detail[0], r.detail[1], r.detail[2]};
+    for (int i = 0; i < n_info; ++i) info[i] = v ? fields[i] : 0;
+    if (drain) return XS_ERR_DEVICE_DRAIN;
+    if (v == 0) return XS_OK;
+    return v == xs::XS_DEVICE_BOUNDS_CODE ? XS_ERR_DEVICE_BOUNDS : XS_ERR_DEVICE_TIMEOUT;
 }
+
+int xs_attn_get_device_error(void* stream) { return xs_attn_get_device_error_info(stream, nullptr, 0); }
 
 const char* xs_attn_error_string(int code) {
     switch (code) {
@@ -795,6 +836,10 @@ const char* xs_attn_error_string(int code) {
         case XS_ERR_UNSUPPORTED_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
         case XS_ERR_WORKSPACE: return "the workspace is smaller than xs_attn_workspace_bytes reports";
         case XS_ERR_LAYOUT: return "unknown output layout";
+        case XS_ERR_DEVICE_DRAIN:
+            return "after an expired wait, a kernel gave up waiting for its own copies or MMAs in flight";
+        case XS_ERR_DEVICE_BOUNDS: return "an index check inside a kernel failed; the access was skipped";
+        case XS_ERR_UNAVAILABLE: return "this variant is disabled in this build";
         default: return "unknown xsattn error code";
     }
 }

@@ -69,6 +69,33 @@
 namespace xs {
 
 __device__ int g_device_error = 0;
+__device__ DeviceErrorInfo g_error_info;
+__device__ int g_drain_failed = 0;
+
+// Records the first device error of the launch (later ones only find the word
+// set).  Out of line: it runs at most once per launch and must not weigh on the
+// register allocation of the loops that call it.
+__device__ __noinline__ void report_error(int code, int site, int d0, int d1, int d2) {
+    if (atomicCAS(&g_device_error, 0, code) == 0) {
+        DeviceErrorInfo r;
+        r.code = code;
+        r.cta = static_cast<int>(blockIdx.x);
+        r.warp = static_cast<int>(threadIdx.x >> 5);
+        r.lane = static_cast<int>(threadIdx.x & 31u);
+        r.site = site;
+        r.detail[0] = d0;
+        r.detail[1] = d1;
+        r.detail[2] = d2;
+        g_error_info = r;
+        __threadfence();
+    }
+}
+
+// Time since t0 has reached the limit.  Signed, so that a timer read that
+// comes out below t0 counts as no time passed rather than as a huge one.
+__device__ __forceinline__ bool expired(uint64_t t0, uint64_t limit_ns) {
+    return static_cast<long long>(globaltimer_ns() - t0) >= static_cast<long long>(limit_ns);
+}
 
 namespace {
 
@@ -123,17 +150,18 @@ struct Cfg {
 // first probe is a non-blocking test; after it the time limit is checked before
 // every further probe, and those probes may suspend the warp (up to 200 us each)
 // instead of spinning.  A limit of 0 therefore gives up at the first wait that
-// is not already over.
+// is not already over.  On expiry the wait records (barrier, parity, piece,
+// block) as the launch's first error, unless one is recorded already.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint64_t timeout_ns) {
+                                          uint64_t timeout_ns, int unit = -1, int blk = -1) {
     bool ok = mbar_test_wait(bar, parity);
     if (!__all_sync(0xffffffffu, ok)) {
         const uint64_t t0 = globaltimer_ns();
         while (!ok) {
             if (*abort_flag) break;
-            if (globaltimer_ns() - t0 >= timeout_ns) {
+            if (expired(t0, timeout_ns)) {
                 *abort_flag = 1;
-                atomicCAS(&g_device_error, 0, XS_DEVICE_TIMEOUT_CODE);
+                report_error(XS_DEVICE_TIMEOUT_CODE, static_cast<int>(bar), static_cast<int>(parity), unit, blk);
                 break;
             }
             ok = mbar_try_wait_sleep(bar, parity, 200000u);
@@ -146,17 +174,33 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // The same bounded wait for a single thread (the issuing lanes of the producer
 // and MMA roles), without warp votes.
 __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                            uint64_t timeout_ns) {
+                                            uint64_t timeout_ns, int unit = -1, int blk = -1) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 >= timeout_ns) {
+        if (expired(t0, timeout_ns)) {
             *abort_flag = 1;
-            atomicCAS(&g_device_error, 0, XS_DEVICE_TIMEOUT_CODE);
+            report_error(XS_DEVICE_TIMEOUT_CODE, static_cast<int>(bar), static_cast<int>(parity), unit, blk);
             return false;
         }
         if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    }
+}
+
+// Wait of the abort path for an asynchronous operation already issued (a TMA
+// copy, the MMAs before a commit): bounded by `limit_ns`; if it gives up, the
+// operation may still be in flight when the CTA frees its tensor memory and
+// exits, so that is flagged for the host (XS_ERR_DEVICE_DRAIN), beside the
+// error that caused the abort.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_test_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(bar, parity, 200000u)) {
+        if (expired(t0, limit_ns)) {
+            atomicOr(&g_drain_failed, 1);
+            return;
+        }
     }
 }
 
@@ -234,8 +278,17 @@ __device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* v
         const long long u = static_cast<long long>(idx) * G + ((idx & 1) ? G - 1 - i : i);
         if (u >= a.units) return false;
         const int t = static_cast<int>(u) / a.H;
+        // index checks on the host-built table (every role takes the same exit)
+        if (t >= vt->n_tiles) {
+            report_error(XS_DEVICE_BOUNDS_CODE, 1, t, vt->n_tiles, idx);
+            return false;
+        }
         const unsigned e = vt->tile[t];
         const int seq = static_cast<int>(e >> 16);
+        if (seq >= vt->n_seqs) {
+            report_error(XS_DEVICE_BOUNDS_CODE, 1, t, static_cast<int>(e), idx);
+            return false;
+        }
         w.b = 0;
         w.row0 = vt->cu[seq];
         w.len = vt->cu[seq + 1] - w.row0;
@@ -248,6 +301,10 @@ __device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* v
             const int v = static_cast<int>(u) - first * a.H;      // unit within the sequence, < nq * H
             w.h = v / nq;
             w.qt = v - w.h * nq;
+        }
+        if (w.row0 < 0 || w.len < 1 || w.row0 + w.len > a.S || w.qt * BLOCK_M >= w.len || w.h < 0 || w.h >= a.H) {
+            report_error(XS_DEVICE_BOUNDS_CODE, 1, t, static_cast<int>(e), w.row0);
+            return false;
         }
         w.k0 = 0;
         w.nb = CAUSAL ? w.qt + 1 : (w.len + BLOCK_N - 1) / BLOCK_N;
@@ -366,7 +423,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         const int b = w.b, h = w.h, qt = w.qt;
         const int qb = u_iter % C::Q_BUFS;
         if (u_iter >= C::Q_BUFS)
-            ok = thread_wait(bar(C::B_Q_FREE + qb), ((u_iter / C::Q_BUFS) - 1) & 1, abort_flag, a.timeout_ns);
+            ok = thread_wait(bar(C::B_Q_FREE + qb), ((u_iter / C::Q_BUFS) - 1) & 1, abort_flag, a.timeout_ns, u_iter);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(C::B_Q_FULL + qb), C::TILE_BYTES);
         const int row_base = VARLEN ? w.row0 : 0;   // packed row of the sequence start
@@ -392,7 +449,8 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
             blk += w.k0;
             const uint32_t stage = item % C::KV_STAGES;
             const uint32_t round = item / C::KV_STAGES;
-            if (round > 0) ok = thread_wait(bar(C::B_KV_FREE + stage), (round - 1) & 1, abort_flag, a.timeout_ns);
+            if (round > 0)
+                ok = thread_wait(bar(C::B_KV_FREE + stage), (round - 1) & 1, abort_flag, a.timeout_ns, u_iter, blk);
             if (!ok) break;
             mbar_arrive_expect_tx(bar(C::B_KV_FULL + stage), C::TILE_BYTES);
             int kv_row;
@@ -406,13 +464,11 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     if (!ok) {
         // Let the copies already issued land before the CTA exits: wait (bounded)
         // for the newest phase of every ring stage used and for the last Q load.
-        volatile int no_abort = 0;
         for (uint32_t back = 1; back <= C::KV_STAGES && back <= item; ++back) {
             const uint32_t it = item - back;
-            thread_wait(bar(C::B_KV_FULL + it % C::KV_STAGES), (it / C::KV_STAGES) & 1, &no_abort, 20000000ull);
+            drain_wait(bar(C::B_KV_FULL + it % C::KV_STAGES), (it / C::KV_STAGES) & 1, 20000000ull);
         }
-        if (q_last >= 0)
-            thread_wait(bar(C::B_Q_FULL + q_last % C::Q_BUFS), (q_last / C::Q_BUFS) & 1, &no_abort, 20000000ull);
+        if (q_last >= 0) drain_wait(bar(C::B_Q_FULL + q_last % C::Q_BUFS), (q_last / C::Q_BUFS) & 1, 20000000ull);
     }
 }
 
@@ -448,15 +504,17 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
         const int n = w.nb;
         const int qb = u_iter % C::Q_BUFS;
         const uint64_t qdesc = desc_add(qdesc0, qb * (C::TILE_BYTES >> 4));
-        ok = thread_wait(bar(C::B_Q_FULL + qb), (u_iter / C::Q_BUFS) & 1, abort_flag, a.timeout_ns);
+        ok = thread_wait(bar(C::B_Q_FULL + qb), (u_iter / C::Q_BUFS) & 1, abort_flag, a.timeout_ns, u_iter);
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gs = g + j;
             const uint32_t sb = gs & 1;
             // the softmax has read this S buffer's previous scores (block gs-2)
-            if (gs >= 2) ok = thread_wait(bar(C::B_S_FREE + sb), ((gs >> 1) - 1) & 1, abort_flag, a.timeout_ns);
+            if (gs >= 2)
+                ok = thread_wait(bar(C::B_S_FREE + sb), ((gs >> 1) - 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
             const uint32_t item = item0 + ring_pos_k(j);
             const uint32_t stage = item % C::KV_STAGES;
-            if (ok) ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns);
+            if (ok)
+                ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns, u_iter, j);
             if (!ok) break;
             tc_fence_after();
             const uint64_t kdesc = desc_add(kdesc0, stage * (C::TILE_BYTES >> 4));
@@ -474,8 +532,7 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
     // Drain: B_DRAIN completes when both issuers' MMAs have all completed (TMEM
     // is freed after it).  The limit is at least 20 ms whatever the wait limit.
     mma_commit(bar(C::B_DRAIN));
-    volatile int no_abort = 0;
-    thread_wait(bar(C::B_DRAIN), 0, &no_abort, a.timeout_ns > 20000000ull ? a.timeout_ns : 20000000ull);
+    drain_wait(bar(C::B_DRAIN), 0, a.timeout_ns > 20000000ull ? a.timeout_ns : 20000000ull);
 }
 
 // Issuer of PV(j): O += P(j) V_j (A = P buffer from TMEM).  One thread.
@@ -497,12 +554,14 @@ __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* s
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gj = g + j;
             const uint32_t pb = gj & 1;
-            ok = thread_wait(bar(C::B_P_FULL + pb), (gj >> 1) & 1, abort_flag, a.timeout_ns);
+            ok = thread_wait(bar(C::B_P_FULL + pb), (gj >> 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
             // the epilogue has read the previous unit's O (PV(0) overwrites it)
-            if (ok && j == 0 && u_iter > 0) ok = thread_wait(bar(C::B_O_FREE), (u_iter - 1) & 1, abort_flag, a.timeout_ns);
+            if (ok && j == 0 && u_iter > 0)
+                ok = thread_wait(bar(C::B_O_FREE), (u_iter - 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
             const uint32_t item = item0 + ring_pos_v(j, n);
             const uint32_t stage = item % C::KV_STAGES;
-            if (ok) ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns);
+            if (ok)
+                ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns, u_iter, j);
             if (!ok) break;
             tc_fence_after();
             const uint64_t vdesc = desc_add(vdesc0, stage * (C::TILE_BYTES >> 4));
@@ -518,27 +577,26 @@ __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* s
         item0 += 2u * n;
     }
     mma_commit(bar(C::B_DRAIN));
-    volatile int no_abort = 0;
-    thread_wait(bar(C::B_DRAIN), 0, &no_abort, a.timeout_ns > 20000000ull ? a.timeout_ns : 20000000ull);
+    drain_wait(bar(C::B_DRAIN), 0, a.timeout_ns > 20000000ull ? a.timeout_ns : 20000000ull);
 }
 
 // ------------------------------------------------------- softmax + epilogue
 // Bounded wait (whole warp) until every softmax warp of CTA `slot` has published
-// its part of a split tile in this launch.  Each lane polls the eight flags
-// itself with acquire loads, so its later loads of the partial are ordered
-// after them.  The result is warp-uniform.
-__device__ __forceinline__ bool wait_partial(const AttnArgs& a, int slot, volatile int* abort_flag) {
+// its part of a split tile in this launch (flag == this launch's epoch).  Each
+// lane polls the eight flags itself with acquire loads, so its later loads of
+// the partial are ordered after them.  The result is warp-uniform.
+__device__ __forceinline__ bool wait_partial(const AttnArgs& a, int slot, unsigned epoch, volatile int* abort_flag) {
     const unsigned* f = a.sp.part_flag + slot * NUM_SOFTMAX_WARPS;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         bool mine = true;
 #pragma unroll
-        for (int i = 0; i < NUM_SOFTMAX_WARPS; ++i) mine = mine && (ld_acquire_gpu(f + i) == a.sp.epoch);
+        for (int i = 0; i < NUM_SOFTMAX_WARPS; ++i) mine = mine && (ld_acquire_gpu(f + i) == epoch);
         if (__all_sync(0xffffffffu, mine)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 >= a.timeout_ns) {
+        if (expired(t0, a.timeout_ns)) {
             *abort_flag = 1;
-            atomicCAS(&g_device_error, 0, XS_DEVICE_TIMEOUT_CODE);
+            report_error(XS_DEVICE_TIMEOUT_CODE, 0x40000 + slot, static_cast<int>(epoch), -1, -1);
             return false;
         }
         __nanosleep(256);
@@ -599,7 +657,7 @@ __device__ __forceinline__ float exp64(const uint32_t (&sr)[2][32], float c, flo
 //              over this piece and the parts.
 template <int D>
 __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, uint32_t o_cols, int row, int half,
-                                            int warp, float m, float l, volatile int* abort_flag) {
+                                            int warp, float m, float l, unsigned epoch, volatile int* abort_flag) {
     constexpr int DH = D / 2;
     if (w.kind == WORK_PART) {
         float* po = a.sp.part_o + (static_cast<size_t>(blockIdx.x) * BLOCK_M + row) * D + half * DH;
@@ -616,7 +674,7 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
         __syncwarp();
         if (lane_id() == 0) {
             __threadfence();
-            st_release_gpu(a.sp.part_flag + blockIdx.x * NUM_SOFTMAX_WARPS + warp, a.sp.epoch);
+            st_release_gpu(a.sp.part_flag + blockIdx.x * NUM_SOFTMAX_WARPS + warp, epoch);
         }
         return true;
     }
@@ -627,7 +685,7 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
     while (j1 < a.sp.sk_ctas && sk_start(a, j1) < tile_end) ++j1;
     float m_all = m;
     for (int j = j0; j < j1; ++j) {
-        if (!wait_partial(a, j, abort_flag)) return false;
+        if (!wait_partial(a, j, epoch, abort_flag)) return false;
         m_all = fmaxf(m_all, a.sp.part_ml[static_cast<size_t>(j) * BLOCK_M + row].x);
     }
     const float f_own = ex2_approx(m - m_all);
@@ -638,12 +696,18 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
     }
     const float inv_l = 1.0f / l_all;
     const int s_row = w.qt * BLOCK_M + row;
-    const bool store = s_row < a.S;
+    bool store = s_row < a.S;
     __nv_bfloat16* dst = nullptr;
     if (store) {
         const int p = s_row / a.epi.Sl + w.h / a.epi.Hl;
-        dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
-              ((static_cast<size_t>(w.b) * a.epi.Sl + s_row % a.epi.Sl) * a.epi.Hl + w.h % a.epi.Hl) * D + half * DH;
+        if (p < MAX_PTRS && a.epi.ptr[p] != nullptr) {
+            dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
+                  ((static_cast<size_t>(w.b) * a.epi.Sl + s_row % a.epi.Sl) * a.epi.Hl + w.h % a.epi.Hl) * D +
+                  half * DH;
+        } else {
+            report_error(XS_DEVICE_BOUNDS_CODE, 2, p, s_row, w.h);
+            store = false;
+        }
     }
 #pragma unroll 1
     for (int q = 0; q < DH / 32; ++q) {
@@ -720,7 +784,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
         float m_run = 0.0f, l_run = 0.0f;
         for (int j = 0; j < n; ++j, ++g) {
             const uint32_t sb = g & 1;
-            ok = warp_wait(bar(C::B_S_FULL + sb), (g >> 1) & 1, abort_flag, a.timeout_ns);
+            ok = warp_wait(bar(C::B_S_FULL + sb), (g >> 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[2][32];
@@ -769,7 +833,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             // Rescale of this thread's half of the O row (rare); PV(g-1) must have
             // completed first.  Warp-uniform: TMEM access is collective.
             if (redo) {
-                ok = warp_wait(bar(C::B_P_FREE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag, a.timeout_ns);
+                ok = warp_wait(bar(C::B_P_FREE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -784,7 +848,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             }
             // P buffer sb is free once PV(g-2) has completed.
             if (g >= 2) {
-                ok = warp_wait(bar(C::B_P_FREE + sb), ((g >> 1) - 1) & 1, abort_flag, a.timeout_ns);
+                ok = warp_wait(bar(C::B_P_FREE + sb), ((g >> 1) - 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -806,7 +870,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
         Work w;
         get_work<CAUSAL, VARLEN>(a, vt, u_iter, w);   // the same piece of work as above (recomputed, not kept live)
         const int b = w.b, h = w.h, qt = w.qt;
-        ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns);
+        ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns, u_iter);
         if (!ok) break;
         tc_fence_after();
         if (w.kind == WORK_FULL) {
@@ -821,9 +885,12 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                 const int p = s_row / a.epi.Sl + h / a.epi.Hl;
                 const int s_dst = s_row % a.epi.Sl;
                 const int h_dst = h % a.epi.Hl;
-                dst_row = reinterpret_cast<unsigned long long>(
-                    reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
-                    ((static_cast<size_t>(b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D + half * DH);
+                if (p < MAX_PTRS && a.epi.ptr[p] != nullptr)
+                    dst_row = reinterpret_cast<unsigned long long>(
+                        reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
+                        ((static_cast<size_t>(b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D + half * DH);
+                else
+                    report_error(XS_DEVICE_BOUNDS_CODE, 2, p, s_row, h);
             }
             uint4* stage = reinterpret_cast<uint4*>(smem + C::STAGE_OFF + warp * 2048);
             const int lane = static_cast<int>(lane_id());
@@ -854,7 +921,8 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                 __syncwarp();   // the stage is rewritten by the next chunk
             }
         } else {
-            ok = split_epilogue<D>(a, w, t_base + O_COL + half * DH, row, half, warp, m_run, l_row, abort_flag);
+            ok = split_epilogue<D>(a, w, t_base + O_COL + half * DH, row, half, warp, m_run, l_row,
+                                   *reinterpret_cast<const volatile unsigned*>(smem + C::MISC_OFF + 8), abort_flag);
             if (!ok) break;
         }
         tc_fence_before();
@@ -894,6 +962,14 @@ __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorM
             mbar_init(bar0 + 8 * (C::B_KV_FREE + s), 1);
         }
         *abort_flag = 0;
+        // this launch's split-tile epoch: one more than the launches finished on
+        // the workspace (never 0, the value of a flag nobody has written)
+        unsigned epoch = 0;
+        if (args.sp.sk_iters != 0) {
+            epoch = *reinterpret_cast<volatile unsigned*>(args.sp.launch_count) + 1u;
+            if (epoch == 0) epoch = 1;
+        }
+        *reinterpret_cast<volatile unsigned*>(smem + C::MISC_OFF + 8) = epoch;
         fence_mbar_init();
     }
     if (warp == WARP_TMA && lane_id() < n_maps) {
@@ -927,6 +1003,16 @@ __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorM
     __syncthreads();
     tc_fence_after();
     if (warp == WARP_MMA_S) tmem_dealloc(tmem_base, TMEM_COLS);
+    // The last CTA of a split launch to get here advances the workspace's launch
+    // count (every CTA has read it by then), so the next launch uses a new epoch.
+    if (threadIdx.x == 0 && args.sp.sk_iters != 0) {
+        __threadfence();
+        if (atomicAdd(args.sp.launch_count + 1, 1u) == gridDim.x - 1) {
+            args.sp.launch_count[1] = 0;
+            __threadfence();
+            atomicAdd(args.sp.launch_count, 1u);
+        }
+    }
 }
 
 template <int D>
@@ -1051,11 +1137,16 @@ template cudaError_t launch_attn<64>(const CUtensorMap&, const CUtensorMap&, con
 template cudaError_t launch_attn<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const AttnArgs&,
                                       int, bool, cudaStream_t);
 
-cudaError_t read_and_clear_device_error(int* value) {
+cudaError_t read_and_clear_device_error(int* value, DeviceErrorInfo* info, int* drain_failed) {
     int zero = 0;
+    DeviceErrorInfo none{};
     cudaError_t e = cudaMemcpyFromSymbol(value, g_device_error, sizeof(int));
-    if (e != cudaSuccess) return e;
-    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(drain_failed, g_drain_failed, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(info, g_error_info, sizeof(DeviceErrorInfo));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_drain_failed, &zero, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_error_info, &none, sizeof(DeviceErrorInfo));
+    return e;
 }
 
 }  // namespace xs

@@ -10,7 +10,19 @@
 namespace xs {
 
 constexpr int MAX_PTRS = 16;              // == XS_MAX_P
-constexpr int XS_DEVICE_TIMEOUT_CODE = 1; // value a kernel writes to the device error word
+// Values a kernel writes to the device error word (the first one wins).
+constexpr int XS_DEVICE_TIMEOUT_CODE = 1; // a bounded wait expired; the launch was abandoned
+constexpr int XS_DEVICE_BOUNDS_CODE = 3;  // a per-piece index check failed; the access was skipped
+// Where the first device error of a launch happened (see report_error).
+struct DeviceErrorInfo {
+    int code;       // XS_DEVICE_*_CODE
+    int cta;        // blockIdx.x
+    int warp;       // threadIdx.x / 32
+    int lane;
+    int site;       // waits: shared-memory address of the mbarrier (split-tile flags: 0x40000 + slot);
+                    // index checks: 1 packed-sequence table entry, 2 destination shard
+    int detail[3];  // waits: phase parity, piece index, key block; index checks: the values checked
+};
 
 // Where each output row (b, s, h) of the attention kernel goes:
 //   p = s / Sl + h / Hl,  ptr[p] + ((b * Sl + s % Sl) * Hl + h % Hl) * D
@@ -30,9 +42,14 @@ struct EpiParams {
 // may start or end inside a tile, and a tile may be cut among several CTAs.
 // Every piece that starts inside a tile (a "part") writes its unnormalised
 // partial result to slot `its CTA index` of the workspace and publishes it with
-// `epoch` in one flag per softmax warp; the piece that starts the tile (the
-// "head", done last by its CTA) waits for the parts of the CTAs after it whose
-// ranges start inside the tile and merges them.  sk_iters == 0: no split.
+// the launch's epoch in one flag per softmax warp; the piece that starts the
+// tile (the "head", done last by its CTA) waits for the parts of the CTAs after
+// it whose ranges start inside the tile and merges them.  sk_iters == 0: no split.
+// The epoch lives in the workspace, not in the launch arguments: launch_count[0]
+// counts the launches that have finished on this workspace, and a launch uses
+// launch_count[0] + 1 (0 skipped), read by every CTA at its start; the last CTA
+// to finish (counted in launch_count[1]) advances it.  A replayed launch
+// therefore never takes flags left by an earlier one for its own.
 struct SplitParams {
     int dp_tiles;
     int sk_ctas;
@@ -40,7 +57,7 @@ struct SplitParams {
     float* part_o;         // [grid][128][D] fp32 partial numerators
     float2* part_ml;       // [grid][128] (running max in log2 units, row sum)
     unsigned* part_flag;   // [grid][8] epoch of the publishing softmax warp
-    unsigned epoch;        // this launch's epoch (never 0)
+    unsigned* launch_count;  // [2]: finished launches, CTAs finished in this launch
 };
 
 struct AttnArgs {
@@ -107,7 +124,10 @@ template <int D>
 cudaError_t launch_attn_sharded(const ShardMaps& maps, int P, const AttnArgs& args, int grid, bool cooperative,
                                 cudaStream_t stream);
 
-cudaError_t read_and_clear_device_error(int* value);
+// Reads and clears the device error word, the record of the first error and the
+// flag of abort drains that gave up (copies or MMAs possibly still in flight when
+// a CTA exited).
+cudaError_t read_and_clear_device_error(int* value, DeviceErrorInfo* info, int* drain_failed);
 
 struct RelayoutArgs {
     const void* heads[MAX_PTRS];

@@ -65,7 +65,11 @@ enum {
     XS_ERR_DEVICE_TIMEOUT = -10, /* a bounded wait inside a kernel ran out; see below   */
     XS_ERR_UNSUPPORTED_DEVICE = -11, /* the current device is not sm_103 (GB300)       */
     XS_ERR_WORKSPACE = -12,      /* the workspace is smaller than required              */
-    XS_ERR_LAYOUT = -13          /* unknown output layout                               */
+    XS_ERR_LAYOUT = -13,         /* unknown output layout                               */
+    XS_ERR_DEVICE_DRAIN = -14,   /* after an expired wait, a copy or MMA may still have
+                                    been in flight when a CTA freed its tensor memory   */
+    XS_ERR_DEVICE_BOUNDS = -15,  /* a kernel's index check failed; the access was skipped */
+    XS_ERR_UNAVAILABLE = -16     /* this variant is disabled in this build (see its entry) */
 };
 
 /* Output layouts of xs_attn_fwd_balanced (the three layouts of the entry points
@@ -210,7 +214,7 @@ int xs_attn_workspace_bytes(int B, int S, int H, int D, size_t* bytes);
  * remaining tiles are divided evenly over all SMs ("stream-K"); a tile whose
  * key range is cut between two CTAs is completed by both: the later CTA writes
  * its unnormalised partial output (fp32), running max and row sum to the
- * workspace and publishes them with a per-launch epoch, the earlier CTA waits
+ * workspace and publishes them with the launch's epoch, the earlier CTA waits
  * for them (a bounded wait) and merges:
  *     O = (O_1 2^(m_1-m) + O_2 2^(m_2-m)) / (l_1 2^(m_1-m) + l_2 2^(m_2-m)),
  *     m = max(m_1, m_2).
@@ -220,11 +224,17 @@ int xs_attn_workspace_bytes(int B, int S, int H, int D, size_t* bytes);
  *                    xs_attn_workspace_bytes(B, S, H, D) bytes, not overlapping
  *                    any input or output; NULL selects the plain schedule.
  *                    Contents: scratch owned by the library during the call.
- *                    It must be zero-filled once before its first use (the
- *                    flags of a launch are recognised by their epoch, and a
- *                    zero flag never matches one).  Two calls may share a
- *                    workspace only if they are ordered (same stream, or
- *                    synchronised); concurrent calls on one workspace race.
+ *                    It must be zero-filled once before its first use, and it
+ *                    keeps state between calls at fixed offsets from its start
+ *                    (a launch count and the flags), so reuse it for any shape
+ *                    at the same address.  A launch takes one more than the
+ *                    launches finished on it as the epoch of its flags, and
+ *                    its last CTA to finish advances the count.  No epoch is
+ *                    baked into the launch arguments, so a launch captured in a
+ *                    CUDA graph and replayed never mistakes an earlier replay's
+ *                    flags for its own.  Two calls may share a workspace only
+ *                    if they are ordered (same stream, or synchronised);
+ *                    concurrent calls on one workspace race.
  *   workspace_bytes  its size in bytes; smaller than required ->
  *                    XS_ERR_WORKSPACE (nothing launched).
  * When a tile is split the kernel is launched cooperatively (all CTAs resident
@@ -297,7 +307,13 @@ int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, 
  *   seqlens   HOST int array of n_seqs lengths, each >= 0 (empty sequences are
  *             skipped), read before the call returns.
  *   n_seqs    1 .. 1024.
- *   causal    0: attend to the whole sequence; otherwise causal within it.
+ *   causal    0: attend to the whole sequence.  Any other value asks for the
+ *             causal form, which this build refuses with XS_ERR_UNAVAILABLE
+ *             before touching any CUDA state: at 75,776 packed tokens (four
+ *             sequences, 40 heads) its launch ended in an unspecified launch
+ *             failure, the cause of which is not established, so it is not
+ *             launched at all.  (Causal attention over one [B, S, H, D] tensor
+ *             is xs_attn_causal_fwd.)
  *   layout    XS_LAYOUT_A2A: outs = P sequence shards [T/P, H, D] of the packed
  *             rows (shard p holds rows [p*T/P, (p+1)*T/P), whichever sequences
  *             they belong to; T % P == 0 and H % P == 0);
@@ -307,12 +323,12 @@ int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, 
  * a sequence at most 8,388,608 rows; tiles x H at most 2^31 - 1.  The library builds the tile list on the
  * host (longest first) and passes it in the launch's parameter space (about
  * 20 KB): the call allocates no device memory.  With equal lengths the result is
- * bit-identical to xs_attn_a2a_fwd / xs_attn_causal_fwd on the [B, S, H, D] view
- * of the same memory.
+ * bit-identical to xs_attn_a2a_fwd on the [B, S, H, D] view of the same memory.
  * Returns XS_OK; XS_ERR_NULL (q, k, v, outs, an out pointer or seqlens);
  * XS_ERR_SHAPE (n_seqs out of range, a negative or too long length, lengths not
- * summing to T, too many tiles or tiles x H, H < 1); the checks of xs_attn_a2a_fwd otherwise
- * (with B = 1, S = T); asynchronous on `stream`.
+ * summing to T, too many tiles or tiles x H, H < 1); XS_ERR_UNAVAILABLE (causal);
+ * the checks of xs_attn_a2a_fwd otherwise (with B = 1, S = T); asynchronous on
+ * `stream`.
  */
 int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* seqlens, int n_seqs,
                        int causal, int layout, void* const* outs, int T, int H, int D, int P, float scale,
@@ -351,12 +367,34 @@ int xs_burst_gap(void* dst, size_t dst_bytes, int producers, size_t burst_bytes,
 
 /*
  * xs_attn_get_device_error -- synchronises `stream`, then reads and clears the
- * library's device error word on the current device.  Returns XS_OK, or
- * XS_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel expired (the kernel
- * then abandoned its work and returned; its outputs are unspecified), or
- * XS_ERR_CUDA if synchronisation itself failed.
+ * library's device error state on the current device (the error word, the
+ * record of the first error and the drain flag).  Returns XS_OK;
+ * XS_ERR_DEVICE_DRAIN if, after an expired wait, a CTA's bounded wait for its
+ * own copies or MMAs in flight also gave up (the CTA then freed its tensor
+ * memory and exited with them possibly outstanding: treat the context as
+ * suspect); else XS_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel expired
+ * (the kernel abandoned its work and returned; its outputs are unspecified);
+ * XS_ERR_DEVICE_BOUNDS if an index check inside a kernel failed (the access was
+ * skipped: an internal error); or XS_ERR_CUDA if synchronisation itself failed.
  */
 int xs_attn_get_device_error(void* stream);
+
+/*
+ * xs_attn_get_device_error_info -- as xs_attn_get_device_error (same return
+ * value, same clearing), and also copies the record of the first device error
+ * since the last clear into info[0 .. n_info) (n_info <= 8; missing fields are
+ * not written; all zero when there was none):
+ *   info[0]  kind: 0 none, 1 expired wait, 3 failed index check
+ *   info[1]  CTA index, info[2] warp, info[3] lane of the thread that recorded it
+ *   info[4]  site: for a wait, the shared-memory address of its mbarrier (the
+ *            split-tile flags of CTA slot s: 0x40000 + s); for an index check,
+ *            1 = packed-sequence table entry, 2 = destination shard
+ *   info[5..7]  details: for a wait, the phase parity, the piece index and the
+ *            key block it waited in (-1: none); for an index check, the values
+ *            that failed it.
+ *   info  host array of n_info ints (may be NULL when n_info == 0).
+ */
+int xs_attn_get_device_error_info(void* stream, int* info, int n_info);
 
 /* Human-readable text for an XS_* code (static storage; never NULL). */
 const char* xs_attn_error_string(int code);

@@ -33,10 +33,11 @@ def test_exports_match_header(xs):
 
 
 def test_error_strings(xs):
-    for code in range(0, -12, -1):
+    default = xs.xs_attn_error_string(-999)
+    assert "unknown" in default
+    for code in range(0, -16, -1):
         s = xs.xs_attn_error_string(code)
-        assert s and "unknown" not in s
-    assert "unknown" in xs.xs_attn_error_string(-999)
+        assert s and s != default
     assert xs.lib.xs_attn_version() >= 100
 
 
@@ -201,6 +202,9 @@ def test_varlen_validation(xs):
     # 1024 one-row sequences are 1024 tiles; with 2**21 + 1 heads the work units
     # (tiles x heads) would overflow an int although the dense-shape limits hold
     assert call([1] * 1024, layout=CONT, P=1, H=2 ** 21 + 1, D=64) == xs.XS_ERR_SHAPE
+    # the causal form is disabled: refused on the host, for any otherwise valid call
+    assert call([100, 156], causal=1) == xs.XS_ERR_UNAVAILABLE
+    assert call([256], causal=7, layout=CONT, P=1) == xs.XS_ERR_UNAVAILABLE
 
 
 def test_workspace_query_validation(xs):
@@ -238,3 +242,11 @@ def test_ulysses_and_inverse_relayout_validation(xs):
     assert lib.xs_relayout_a2a_inverse(qs, outs, 1, 256, 3, 64, 2, None) == xs.XS_ERR_DIVISIBILITY
     assert lib.xs_relayout_a2a_inverse(qs, _outs(2, base=0x10_0000_0000 + 4096), 1, 256, 2, 64, 2, None) == \
         xs.XS_ERR_OVERLAP
+
+
+def test_device_error_info_arguments_checked_before_any_cuda_call(xs):
+    import ctypes
+    info = (ctypes.c_int * 8)()
+    assert xs.lib.xs_attn_get_device_error_info(None, info, 9) == xs.XS_ERR_NULL
+    assert xs.lib.xs_attn_get_device_error_info(None, None, 1) == xs.XS_ERR_NULL
+    assert xs.lib.xs_attn_get_device_error_info(None, info, -1) == xs.XS_ERR_NULL

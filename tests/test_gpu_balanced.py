@@ -258,3 +258,35 @@ def test_staged_host_entry_with_workspace_matches_device_entry(xs):
     assert xs.xs_attn_get_device_error() == xs.XS_OK
     for a, b in zip(out_h, ref):
         assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
+
+
+def test_balanced_graph_replay_takes_only_its_own_flags(xs):
+    """One split launch captured in a CUDA graph and replayed three times with
+    different inputs copied into the captured buffers: every replay must merge
+    the partial results of its own launch only.  The flags' epoch comes from the
+    workspace's launch count, not from the captured arguments, so each replay
+    matches an uncaptured call on the same inputs bit for bit."""
+    S, D, P, B, H = SHAPES[0]
+    _check_splits(B, S, H)
+    ws = xs.Workspace(xs.xs_attn_workspace_bytes(B, S, H, D))
+    wa = di.Workload("ga", B=B, H=H, S=S, D=D, P=P, scale=1 / math.sqrt(D), seed=31)
+    wb = di.Workload("gb", B=B, H=H, S=S, D=D, P=P, scale=1 / math.sqrt(D), seed=32)
+    a = [bits_to_torch(x) for x in di.random_qkv(wa)]
+    b = [bits_to_torch(x) for x in di.random_qkv(wb)]
+    ref_a = _run(xs, *a, wa.scale, P, ws)
+    ref_b = _run(xs, *b, wa.scale, P, ws)
+    q, k, v = (torch.empty_like(x) for x in a)
+    outs = _shards(B, S, H, D, P)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_A2A, outs, wa.scale, ws)
+    for src, ref in ((a, ref_a), (b, ref_b), (a, ref_a)):
+        for dst, x in zip((q, k, v), src):
+            dst.copy_(x)
+        for o in outs:
+            o.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert xs.xs_attn_get_device_error() == xs.XS_OK
+        for x, y in zip(outs, ref):
+            assert torch.equal(x.view(torch.int16), y.view(torch.int16))

@@ -33,8 +33,14 @@ def test_expired_wait_is_reported_and_context_survives(xs, monkeypatch):
 
     monkeypatch.setenv("XSATTN_WAIT_TIMEOUT_NS", "0")
     xs.xs_attn_a2a_fwd(q, k, v, outs, w.scale)          # the launch itself succeeds
-    assert xs.xs_attn_get_device_error() == xs.XS_ERR_DEVICE_TIMEOUT
-    assert xs.xs_attn_get_device_error() == xs.XS_OK    # the word was cleared
+    code, rec = xs.xs_attn_get_device_error_info()
+    assert code == xs.XS_ERR_DEVICE_TIMEOUT
+    # the record names the wait: a CTA of the 32-tile grid, one of its 12 warps,
+    # an mbarrier address in shared memory, a parity and the piece it waited in
+    assert rec["kind"] == 1
+    assert 0 <= rec["cta"] < 32 and 0 <= rec["warp"] < 12 and 0 <= rec["lane"] < 32
+    assert 0 < rec["site"] < 232448 and rec["detail0"] in (0, 1) and rec["detail1"] >= 0
+    assert xs.xs_attn_get_device_error_info() == (xs.XS_OK, {k: 0 for k in rec})   # cleared
     monkeypatch.delenv("XSATTN_WAIT_TIMEOUT_NS")
 
     torch.cuda.synchronize()                            # the context is intact
