@@ -505,6 +505,69 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """The sequence sweep (B=2, H=16, D=128, P=8, S = 1024 ... 131072 doubling): at
+    each S the fused call, the same kernel storing contiguously (attention alone)
+    and the same kernel into head shards followed by the separate re-layout kernel,
+    interleaved run by run with L2 flushed before each; medians and p10/p90."""
+    import torch
+
+    import dit_attention_ulysses_gb300 as xs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    runs = max(20, args.steps)
+    sampler = ClockSampler(0)
+    sampler.start()
+    t0 = time.time()
+    points = []
+    for S in di.SWEEP_S:
+        w = di.sweep_workload(S)
+        B, H, D, P = w.B, w.H, w.D, w.P
+        q, k, v = (to_device(x, torch, dev) for x in di.random_qkv(w))
+        outs = [torch.empty((B, S // P, H, D), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        contig = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+        heads = [torch.empty((B, S, H // P, D), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        serial = [torch.empty((B, S // P, H, D), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        ws = xs.Workspace.for_shape(B, S, H, D, device=dev) if args.schedule == "balanced" else None
+        fused = lambda: xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_A2A, outs, w.scale, ws, stream)
+        alone = lambda: xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_CONTIGUOUS, [contig], w.scale, ws, stream)
+
+        def serial_path():
+            xs.xs_attn_fwd_balanced(q, k, v, xs.XS_LAYOUT_HEADS, heads, w.scale, ws, stream)
+            xs.xs_relayout_a2a(heads, serial, stream)
+
+        for fn in (fused, alone, serial_path):
+            for _ in range(3):
+                fn()
+        tf, ta, ts = [], [], []
+        for _ in range(runs):
+            tf += time_steps(torch, fused, 1, flush, stream)
+            ta += time_steps(torch, alone, 1, flush, stream)
+            ts += time_steps(torch, serial_path, 1, flush, stream)
+        if xs.xs_attn_get_device_error(stream) != 0:
+            raise RuntimeError(f"device error in the sweep at S={S}")
+        mf, ma, ms_ = statistics.median(tf), statistics.median(ta), statistics.median(ts)
+        points.append({"S": S, "flops": w.flops, "fused_ms": step_percentiles(tf), "alone_ms": step_percentiles(ta),
+                       "alone_plus_relayout_ms": step_percentiles(ts),
+                       "fused_tflops": w.flops / (mf * 1e-3) / 1e12,
+                       "overhead_pct": 100.0 * (mf - ma) / ma, "serial_over_fused": ms_ / mf,
+                       "schedule": "split" if ws is not None else "whole tiles"})
+        del q, k, v, outs, contig, heads, serial, ws
+        torch.cuda.empty_cache()
+    clocks = sampler.stop(t0, time.time())
+    peak_tflops, _, peak_kind = measured_peaks()
+    for pt in points:
+        pt["frac_of_peak"] = pt["fused_tflops"] / peak_tflops
+    print(json.dumps({"sweep": points, "runs_per_point": runs, "statistic": "median (p10/p90 beside it)",
+                      "order": "interleaved fused / alone / alone + re-layout, L2 flushed before each",
+                      "B": 2, "H": 16, "D": 128, "P": 8, "peak_tflops": peak_tflops,
+                      "peak_kind": f"{peak_kind} bf16 burst", "clocks": clocks,
+                      "kernel_source": kernel_source_hash()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -518,12 +581,19 @@ def main():
                          "plain: whole tiles only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the sequence sweep (fused, attention alone, attention + re-layout at every S) "
+                         "and print it as one JSON record instead of the benchmark line")
     args = ap.parse_args()
     rank, world, local_rank = env_rank()
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args, rank, world)   # rank 0 only; other ranks exit without work
+        return
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
         return
     if world > 1:
         import torch.distributed as dist

@@ -27,6 +27,7 @@ __all__ = [
     "xs_relayout_a2a",
     "xs_relayout_a2a_inverse",
     "xs_attn_ulysses_fwd",
+    "xs_attn_ulysses_rank_fwd",
     "xs_burst_gap",
     "xs_attn_a2a_fwd_staged",
     "xs_attn_workspace_bytes",
@@ -94,6 +95,8 @@ EXPORTS = {
                                    ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _f32, _vp, _size, _vp]),
     "xs_relayout_a2a_inverse": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int, _int, _int, _int,
                                        _vp]),
+    "xs_attn_ulysses_rank_fwd": (_int, [_vp, _vp, _vp, ctypes.POINTER(_vp), _int, _int, _int, _int, _int, _int, _f32,
+                                        _vp, _size, _vp]),
     "xs_burst_gap": (_int, [_vp, _size, _int, _size, _int, ctypes.c_longlong, ctypes.c_longlong, _vp, _vp]),
     "xs_attn_get_device_error": (_int, [_vp]),
     "xs_attn_get_device_error_info": (_int, [_vp, ctypes.POINTER(_int), _int]),
@@ -204,6 +207,22 @@ def xs_attn_ulysses_fwd(q_shards, k_shards, v_shards, out_shards, scale: float, 
     _check(lib.xs_attn_ulysses_fwd(_ptr_array([x.data_ptr() for x in qs]), _ptr_array([x.data_ptr() for x in ks]),
                                    _ptr_array([x.data_ptr() for x in vs]), _ptr_array([x.data_ptr() for x in os_]),
                                    B, Sl * P, H, D, P, scale, wp, wn, _stream_handle(stream)), "xs_attn_ulysses_fwd")
+
+
+def xs_attn_ulysses_rank_fwd(q_heads, k_heads, v_heads, out_shard_ptrs, H: int, rank: int, scale: float,
+                             workspace=None, stream=None) -> None:
+    """Attention of Ulysses rank ``rank`` over its head shard [B,S,H/P,D] (q, k, v), storing
+    every output row straight into ``out_shard_ptrs[p]`` (device addresses of the P ranks'
+    sequence shards [B,S/P,H,D], which may belong to other processes) at global head
+    rank*H/P + j.  ``out_shard_ptrs``: ints (device pointers) or CUDA tensors."""
+    B, S, Hl, D = _bshd(q_heads, "q_heads").shape
+    _bshd(k_heads, "k_heads"), _bshd(v_heads, "v_heads")
+    ptrs = [p if isinstance(p, int) else _bshd(p, "out_shards").data_ptr() for p in out_shard_ptrs]
+    P = len(ptrs)
+    wp, wn = _ws(workspace)
+    _check(lib.xs_attn_ulysses_rank_fwd(q_heads.data_ptr(), k_heads.data_ptr(), v_heads.data_ptr(), _ptr_array(ptrs),
+                                        B, S, H, D, P, rank, scale, wp, wn, _stream_handle(stream)),
+           "xs_attn_ulysses_rank_fwd")
 
 
 def xs_relayout_a2a_inverse(seq_shards, heads, stream=None) -> None:

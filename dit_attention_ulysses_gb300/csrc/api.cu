@@ -283,23 +283,35 @@ bool causal_head_major(int BH, int n_qt, int grid) {
 
 // causal: row s attends to keys 0 .. s (one tensor per operand, plain schedule
 // in the kernel's causal tile order; ws is not used).
+// Head range: the launch computes heads [h0, h0 + Hg) of input tensors with H
+// heads (Hg = 0: all of them) and stores head h0 + h at head h0_out + h of the
+// output layout (h0_out < 0: the same as h0); the schedule is planned for the
+// Hg heads.  ws_optional: a workspace too small for the plan selects whole tiles
+// instead of an error.
 int run_attention(const void* q, const void* k, const void* v, const void* const* shards, int P,
                   const xs::EpiParams& epi, int B, int S, int H, int D, float scale, void* ws, size_t ws_bytes,
-                  cudaStream_t stream, bool causal = false) {
+                  cudaStream_t stream, bool causal = false, int h0 = 0, int Hg = 0, bool ws_optional = false,
+                  int h0_out = -1) {
     DeviceInfo dev;
     int rc = device_info(&dev);
     if (rc != XS_OK) return rc;
-    const Plan pl = make_plan(B, S, H, D, dev);
-    const bool split = !causal && ws != nullptr && pl.split;
-    if (split && ws_bytes < pl.ws_bytes) return XS_ERR_WORKSPACE;
+    const int Hw = Hg > 0 ? Hg : H;
+    const Plan pl = make_plan(B, S, Hw, D, dev);
+    bool split = !causal && ws != nullptr && pl.split;
+    if (split && ws_bytes < pl.ws_bytes) {
+        if (!ws_optional) return XS_ERR_WORKSPACE;
+        split = false;
+    }
     xs::AttnArgs a;
     std::memset(&a, 0, sizeof a);
     a.B = B;
     a.S = S;
-    a.H = H;
+    a.H = Hw;
+    a.h0 = h0;
+    a.h0_out = h0_out < 0 ? h0 : h0_out;
     a.n_kv = (S + 127) / 128;
     a.n_qt = (S + 127) / 128;
-    a.units = B * H * a.n_qt;
+    a.units = B * Hw * a.n_qt;
     a.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.epi = epi;
     a.timeout_ns = timeout_ns();
@@ -317,7 +329,7 @@ int run_attention(const void* q, const void* k, const void* v, const void* const
         a.sp.dp_tiles = a.units;
         grid = a.units < dev.sms ? a.units : dev.sms;
     }
-    if (causal) a.causal_head_major = causal_head_major(B * H, a.n_qt, grid) ? 1 : 0;
+    if (causal) a.causal_head_major = causal_head_major(B * Hw, a.n_qt, grid) ? 1 : 0;
     cudaError_t e;
     if (shards) {
         static thread_local xs::ShardMaps maps;   // 6 KB: kept off the stack
@@ -483,6 +495,42 @@ int noalloc_scratch(void** out) {
         s.addr = p;
     }
     *out = s.addr;
+    return XS_OK;
+}
+
+// Streams and events of the host-buffer pipeline (xs_attn_a2a_fwd_staged):
+// created once per device on first use and kept for the life of the process.
+constexpr int PIPE_MAX_GROUPS = 8;
+struct PipeStreams {
+    bool ready = false;
+    std::mutex mutex;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in_done[PIPE_MAX_GROUPS] = {}, kernel_done[PIPE_MAX_GROUPS] = {};
+};
+PipeStreams g_pipe[MAX_DEVICES];
+std::mutex g_pipe_mutex;
+
+int pipe_streams(PipeStreams** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= MAX_DEVICES) return XS_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    PipeStreams& p = g_pipe[dev];
+    if (!p.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if ((e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaEventCreateWithFlags(&p.start, ef)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaEventCreateWithFlags(&p.done, ef)) != cudaSuccess) return cuda_fail(e);
+        for (int g = 0; g < PIPE_MAX_GROUPS; ++g) {
+            if ((e = cudaEventCreateWithFlags(&p.in_done[g], ef)) != cudaSuccess) return cuda_fail(e);
+            if ((e = cudaEventCreateWithFlags(&p.kernel_done[g], ef)) != cudaSuccess) return cuda_fail(e);
+        }
+        p.ready = true;
+    }
+    *out = &p;
     return XS_OK;
 }
 
@@ -666,6 +714,38 @@ int xs_attn_ulysses_fwd(const void* const* q_shards, const void* const* k_shards
                          static_cast<cudaStream_t>(stream));
 }
 
+int xs_attn_ulysses_rank_fwd(const void* q_heads, const void* k_heads, const void* v_heads, void* const* out_shards,
+                             int B, int S, int H, int D, int P, int rank, float scale, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (!q_heads || !k_heads || !v_heads || !out_shards) return XS_ERR_NULL;
+    int rc = check_shape(B, S, H, D, P, true);
+    if (rc != XS_OK) return rc;
+    if (rank < 0 || rank >= P) return XS_ERR_SHAPE;
+    for (int p = 0; p < P; ++p)
+        if (!out_shards[p]) return XS_ERR_NULL;
+    if ((rc = check_scale(scale)) != XS_OK) return rc;
+    if (!aligned16(q_heads) || !aligned16(k_heads) || !aligned16(v_heads)) return XS_ERR_ALIGNMENT;
+    for (int p = 0; p < P; ++p)
+        if (!aligned16(out_shards[p])) return XS_ERR_ALIGNMENT;
+    const int Hl = H / P;
+    const int64_t in_bytes = static_cast<int64_t>(B) * S * Hl * D * 2;
+    const int64_t shard_bytes = static_cast<int64_t>(B) * (S / P) * H * D * 2;
+    Range ins[3] = {range_of(q_heads, in_bytes), range_of(k_heads, in_bytes), range_of(v_heads, in_bytes)};
+    Range outs[XS_MAX_P];
+    for (int p = 0; p < P; ++p) outs[p] = range_of(out_shards[p], shard_bytes);
+    if ((rc = check_disjoint(outs, P, ins, 3)) != XS_OK) return rc;
+    if ((rc = check_workspace(workspace, workspace_bytes, q_heads, k_heads, v_heads, out_shards, P, shard_bytes, B, S,
+                              Hl, D)) != XS_OK)
+        return rc;
+    xs::EpiParams epi;
+    std::memset(&epi, 0, sizeof epi);
+    for (int p = 0; p < P; ++p) epi.ptr[p] = out_shards[p];
+    epi.Sl = S / P;
+    epi.Hl = H;
+    return run_attention(q_heads, k_heads, v_heads, nullptr, 0, epi, B, S, Hl, D, scale, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream), false, 0, 0, false, rank * Hl);
+}
+
 int xs_relayout_a2a_inverse(const void* const* seq_shards, void* const* heads, int B, int S, int H, int D, int P,
                             void* stream) {
     if (!seq_shards || !heads) return XS_ERR_NULL;
@@ -756,19 +836,49 @@ int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v
     if ((rc = check_workspace(workspace, workspace_bytes, q_dev, k_dev, v_dev, out_dev, n_out, shard_bytes, B, S, H,
                               D)) != XS_OK)
         return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t in_bytes = static_cast<size_t>(B) * S * H * D * 2;
+    PipeStreams* ps = nullptr;
+    if ((rc = pipe_streams(&ps)) != XS_OK) return rc;
+    std::lock_guard<std::mutex> lock(ps->mutex);   // one call's enqueues at a time on the shared streams
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    xs::EpiParams epi;
+    std::memset(&epi, 0, sizeof epi);
+    for (int p = 0; p < P; ++p) epi.ptr[p] = out_dev[p];
+    epi.Sl = S / P;
+    epi.Hl = H;
+    // Head groups: the copies of group g + 1 in and of group g - 1 out overlap the
+    // kernel of group g.  Every copy is one pitched cudaMemcpy2DAsync: the group's
+    // heads are hg * D contiguous elements of every [.., H, D] row.
+    const int ng = H < PIPE_MAX_GROUPS ? H : PIPE_MAX_GROUPS;
+    const size_t row = static_cast<size_t>(H) * D * 2;       // bytes per (b, s) row
+    const size_t rows_in = static_cast<size_t>(B) * S, rows_out = static_cast<size_t>(B) * (S / P);
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(q_dev, q_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMemcpyAsync(k_dev, k_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMemcpyAsync(v_dev, v_host, in_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) return cuda_fail(e);
-    if ((rc = xs_attn_fwd_balanced(q_dev, k_dev, v_dev, XS_LAYOUT_A2A, out_dev, B, S, H, D, P, scale, workspace,
-                                   workspace_bytes, stream)) != XS_OK)
-        return rc;
-    for (int p = 0; p < P; ++p)
-        if ((e = cudaMemcpyAsync(out_host[p], out_dev[p], static_cast<size_t>(shard_bytes), cudaMemcpyDeviceToHost,
-                                 st)) != cudaSuccess)
-            return cuda_fail(e);
+    if ((e = cudaEventRecord(ps->start, st)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(ps->in, ps->start, 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(ps->out, ps->start, 0)) != cudaSuccess) return cuda_fail(e);
+    const void* hin[3] = {q_host, k_host, v_host};
+    void* din[3] = {q_dev, k_dev, v_dev};
+    for (int g = 0; g < ng; ++g) {
+        const int h_lo = H * g / ng, h_hi = H * (g + 1) / ng;
+        const size_t off = static_cast<size_t>(h_lo) * D * 2, width = static_cast<size_t>(h_hi - h_lo) * D * 2;
+        for (int t = 0; t < 3; ++t)
+            if ((e = cudaMemcpy2DAsync(static_cast<char*>(din[t]) + off, row, static_cast<const char*>(hin[t]) + off,
+                                       row, width, rows_in, cudaMemcpyHostToDevice, ps->in)) != cudaSuccess)
+                return cuda_fail(e);
+        if ((e = cudaEventRecord(ps->in_done[g], ps->in)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaStreamWaitEvent(st, ps->in_done[g], 0)) != cudaSuccess) return cuda_fail(e);
+        if ((rc = run_attention(q_dev, k_dev, v_dev, nullptr, 0, epi, B, S, H, D, scale, workspace, workspace_bytes,
+                                st, false, h_lo, h_hi - h_lo, true)) != XS_OK)
+            return rc;
+        if ((e = cudaEventRecord(ps->kernel_done[g], st)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaStreamWaitEvent(ps->out, ps->kernel_done[g], 0)) != cudaSuccess) return cuda_fail(e);
+        for (int p = 0; p < P; ++p)
+            if ((e = cudaMemcpy2DAsync(static_cast<char*>(out_host[p]) + off, row,
+                                       static_cast<const char*>(out_dev[p]) + off, row, width, rows_out,
+                                       cudaMemcpyDeviceToHost, ps->out)) != cudaSuccess)
+                return cuda_fail(e);
+    }
+    if ((e = cudaEventRecord(ps->done, ps->out)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(st, ps->done, 0)) != cudaSuccess) return cuda_fail(e);
     return XS_OK;
 }
 

@@ -11,8 +11,9 @@
 // Kernel organisation (one persistent CTA per SM, 12 warps; warp w runs on SM
 // sub-partition w % 4):
 //   warps 0-7  softmax + epilogue of the current 128-row Q tile; two threads per
-//              row: warp w owns rows 32*(w%4) .. +31 (its TMEM lane quarter) and
-//              key columns 64*(w/4) .. +63 of every score block
+//              row, both in one warp: warp w owns the 16 rows 32*(w%4) + 16*(w/4)
+//              .. +15 (half of its TMEM lane quarter); lane i takes key columns
+//              64*(i/16) .. +63 of row i%16 of every score block
 //   warp  8    idle (keeps the three single-thread roles on three different
 //              sub-partitions without changing the register budget: at most
 //              three warps per sub-partition either way)
@@ -45,8 +46,9 @@
 // (PV(j-2)) and in the rare O rescale (PV(j-1)).
 //
 // Softmax (base 2, c = scale*log2(e) folded into one FMA, MUFU ex2):
-//   each thread takes the max of its 64 scores; the two threads of a row combine
-//   them through shared memory and a per-warp-pair mbarrier (a bounded wait);
+//   each thread takes the max of its 64 scores; the two threads of a row are
+//   lanes i and i + 16 of one warp (TMEM 16x32bx2 accesses) and combine them with
+//   one shuffle;
 //   lazy rescale: the running max moves (and O, l are multiplied by
 //   2^(m_run - m_new)) only when the block max exceeds it by more than 8;
 //   p = 2^(s*c - m) -> bf16 -> TMEM P buffer; l accumulates the fp32 p.
@@ -121,10 +123,7 @@ struct Cfg {
     static constexpr int KV_STAGES = (D == 128) ? 5 : 10;
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = Q_BUFS * TILE_BYTES;
-    static constexpr int XCH_OFF = KV_OFF + KV_STAGES * TILE_BYTES;  // row max / row sum exchange
-    static constexpr int XMAX_BYTES = 2 * 2 * BLOCK_M * 4;           // [block parity][half][row] fp32
-    static constexpr int XCH_BYTES = XMAX_BYTES + 2 * BLOCK_M * 4;   // + sums [half][row]
-    static constexpr int STAGE_OFF = XCH_OFF + XCH_BYTES;            // epilogue staging, 2 KB per softmax warp
+    static constexpr int STAGE_OFF = KV_OFF + KV_STAGES * TILE_BYTES;  // epilogue staging, 2 KB per softmax warp
     static constexpr int STAGE_BYTES = NUM_SOFTMAX_WARPS * 2048;
     static constexpr int BAR_OFF = STAGE_OFF + STAGE_BYTES;
     // barrier indices
@@ -137,10 +136,9 @@ struct Cfg {
     static constexpr int B_O_FINAL = 12;               // [1]  MMA -> epilogue
     static constexpr int B_O_FREE = 13;                // [1]  epilogue -> MMA
     static constexpr int B_DRAIN = 14;                 // [1]  both issuers
-    static constexpr int B_PAIR = 15;                  // [4]  the two softmax warps of a lane quarter
-    static constexpr int B_KV_FULL = 19;               // [NS] TMA -> MMA
-    static constexpr int B_KV_FREE = 19 + KV_STAGES;   // [NS] MMA -> TMA
-    static constexpr int NUM_BARS = 19 + 2 * KV_STAGES;
+    static constexpr int B_KV_FULL = 15;               // [NS] TMA -> MMA
+    static constexpr int B_KV_FREE = 15 + KV_STAGES;   // [NS] MMA -> TMA
+    static constexpr int NUM_BARS = 15 + 2 * KV_STAGES;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
@@ -431,7 +429,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
         const CUtensorMap* q_map = pick_map(a, tq, row_base + qt * BLOCK_M, q_row);
         for (int pnl = 0; pnl < C::PANELS; ++pnl)
             tma_load_4d(sbase + C::Q_OFF + qb * C::TILE_BYTES + pnl * PANEL_BYTES, q_map, bar(C::B_Q_FULL + qb),
-                        pnl * 64, h, q_row, b);
+                        pnl * 64, a.h0 + h, q_row, b);
         q_last = u_iter;
         {   // start the next piece's Q towards L2: its load waits for this piece's
             // last S MMA (one Q buffer at D = 128) and then hits L2, not HBM
@@ -439,7 +437,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
             if (get_work<CAUSAL, VARLEN>(a, vt, u_iter + 1, wn)) {
                 int r;
                 const CUtensorMap* m = pick_map(a, tq, (VARLEN ? wn.row0 : 0) + wn.qt * BLOCK_M, r);
-                for (int pnl = 0; pnl < C::PANELS; ++pnl) tma_prefetch_l2_4d(m, pnl * 64, wn.h, r, wn.b);
+                for (int pnl = 0; pnl < C::PANELS; ++pnl) tma_prefetch_l2_4d(m, pnl * 64, a.h0 + wn.h, r, wn.b);
             }
         }
         for (int i = 0; i < 2 * w.nb && ok; ++i) {
@@ -457,7 +455,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
             const CUtensorMap* kv_map = pick_map(a, is_v ? tv : tk, row_base + blk * BLOCK_N, kv_row);
             for (int pnl = 0; pnl < C::PANELS; ++pnl)
                 tma_load_4d(sbase + C::KV_OFF + stage * C::TILE_BYTES + pnl * PANEL_BYTES, kv_map,
-                            bar(C::B_KV_FULL + stage), pnl * 64, h, kv_row, b);
+                            bar(C::B_KV_FULL + stage), pnl * 64, a.h0 + h, kv_row, b);
             ++item;
         }
     }
@@ -646,9 +644,10 @@ __device__ __forceinline__ float exp64(const uint32_t (&sr)[2][32], float c, flo
 
 // Epilogue of a piece of a split tile (rare: at most two per CTA and launch),
 // kept out of line so that it does not weigh on the register allocation of the
-// softmax loop.  The calling thread owns query row `row` of the tile and the DH
-// output columns at TMEM address o_cols (half `half` of the row); m, l are the
-// row's running max (log2 units) and sum over this piece's key blocks.
+// softmax loop.  The calling thread owns query row `row` of the tile and its DH
+// output columns of half `half`, which it reads with the 16x32bx2 TMEM accesses
+// at o_base (the O accumulator at the warp's lanes); m, l are the row's running
+// max (log2 units) and sum over this piece's key blocks.
 //   WORK_PART: publish the unnormalised O, m and l in this CTA's workspace slot,
 //              then this warp's flag (release) with the launch epoch.
 //   WORK_HEAD: wait for the parts of the tile (slots of the following CTAs whose
@@ -656,7 +655,7 @@ __device__ __forceinline__ float exp64(const uint32_t (&sr)[2][32], float c, flo
 //              (sum_k O_k 2^(m_k - M)) / (sum_k l_k 2^(m_k - M)),  M = max_k m_k,
 //              over this piece and the parts.
 template <int D>
-__device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, uint32_t o_cols, int row, int half,
+__device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, uint32_t o_base, int row, int half,
                                             int warp, float m, float l, unsigned epoch, volatile int* abort_flag) {
     constexpr int DH = D / 2;
     if (w.kind == WORK_PART) {
@@ -664,7 +663,7 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
 #pragma unroll 1
         for (int q = 0; q < DH / 32; ++q) {
             uint32_t orr[32];
-            tmem_ld32(o_cols + q * 32, orr);
+            tmem_ld16x2_32<DH>(o_base + q * 32, orr);
             tmem_wait_ld();
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
@@ -699,10 +698,11 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
     bool store = s_row < a.S;
     __nv_bfloat16* dst = nullptr;
     if (store) {
-        const int p = s_row / a.epi.Sl + w.h / a.epi.Hl;
+        const int hg = a.h0_out + w.h;   // head in the output layout
+        const int p = s_row / a.epi.Sl + hg / a.epi.Hl;
         if (p < MAX_PTRS && a.epi.ptr[p] != nullptr) {
             dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
-                  ((static_cast<size_t>(w.b) * a.epi.Sl + s_row % a.epi.Sl) * a.epi.Hl + w.h % a.epi.Hl) * D +
+                  ((static_cast<size_t>(w.b) * a.epi.Sl + s_row % a.epi.Sl) * a.epi.Hl + hg % a.epi.Hl) * D +
                   half * DH;
         } else {
             report_error(XS_DEVICE_BOUNDS_CODE, 2, p, s_row, w.h);
@@ -712,7 +712,7 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
 #pragma unroll 1
     for (int q = 0; q < DH / 32; ++q) {
         uint32_t orr[32];
-        tmem_ld32(o_cols + q * 32, orr);
+        tmem_ld16x2_32<DH>(o_base + q * 32, orr);
         tmem_wait_ld();
         float acc[32];
 #pragma unroll
@@ -747,22 +747,14 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
     using C = Cfg<D>;
     constexpr int DH = D / 2;  // O columns owned by each of a row's two threads
     const int warp = threadIdx.x >> 5;
+    const int lane = static_cast<int>(lane_id());
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-    const int half = warp >> 2;               // key columns [64*half, 64*half + 64)
-    const int row = quarter * 32 + static_cast<int>(lane_id());
-    const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* xmax = reinterpret_cast<float*>(smem + C::XCH_OFF);                   // [2][2][128]
-    float* xsum = reinterpret_cast<float*>(smem + C::XCH_OFF + C::XMAX_BYTES);  // [2][128]
+    const int half = lane >> 4;               // key columns [64*half, 64*half + 64), O columns [DH*half, +DH)
+    // rows 32*quarter + 16*(warp/4) .. +15: the warp's half of its lane quarter
+    const int row = quarter * 32 + (warp >> 2) * 16 + (lane & 15);
+    const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32 + (warp >> 2) * 16) << 16);
     auto bar = [&](int i) { return bar0 + static_cast<uint32_t>(i) * 8u; };
     const float c = a.c;
-    // Exchange with the other thread of this row (the warp 4 apart): both
-    // threads have stored their value to shared memory before either reads.
-    uint32_t xchg = 0;
-    auto xslot = [&]() { return xmax + (xchg & 1) * 2 * BLOCK_M; };
-    auto pair_exchange = [&]() -> bool {
-        warp_arrive(bar(C::B_PAIR + quarter));
-        return warp_wait(bar(C::B_PAIR + quarter), (xchg++) & 1, abort_flag, a.timeout_ns);
-    };
 
     uint32_t g = 0;
     int u_iter = 0;
@@ -788,8 +780,8 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[2][32];
-            tmem_ld32(t_base + S_COL + sb * 128u + half * 64, sr[0]);
-            tmem_ld32(t_base + S_COL + sb * 128u + half * 64 + 32, sr[1]);
+            tmem_ld16x2_32<64>(t_base + S_COL + sb * 128u, sr[0]);
+            tmem_ld16x2_32<64>(t_base + S_COL + sb * 128u + 32, sr[1]);
             tmem_wait_ld();
             tc_fence_before();
             warp_arrive(bar(C::B_S_FREE + sb));  // the MMA may now overwrite this S buffer
@@ -806,15 +798,9 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                     for (int i = 0; i < 32; ++i)
                         if (half * 64 + q * 32 + i >= valid) sr[q][i] = 0xff800000u;  // -inf
             }
-            // Exchange slots alternate with every exchange: a thread writes a slot
-            // again only after the next exchange, which its partner joins only after
-            // reading the slot.
-            // row max: combine the two halves of the row
-            float* xm = xslot();
-            xm[half * BLOCK_M + row] = max64(sr);
-            ok = pair_exchange();
-            if (!ok) break;
-            const float m_blk = fmaxf(xm[row], xm[BLOCK_M + row]) * c;
+            // row max: the two halves of the row are lanes i and i ^ 16
+            const float m_half = max64(sr);
+            const float m_blk = fmaxf(m_half, __shfl_xor_sync(0xffffffffu, m_half, 16)) * c;
             float m_use, alpha = 1.0f;
             bool rescale = false;
             if (j == 0) {
@@ -839,11 +825,11 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
 #pragma unroll
                 for (int q = 0; q < DH / 32; ++q) {
                     uint32_t orr[32];
-                    tmem_ld32(t_base + O_COL + half * DH + q * 32, orr);
+                    tmem_ld16x2_32<DH>(t_base + O_COL + q * 32, orr);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-                    tmem_st32(t_base + O_COL + half * DH + q * 32, orr);
+                    tmem_st16x2_32<DH>(t_base + O_COL + q * 32, orr);
                 }
             }
             // P buffer sb is free once PV(g-2) has completed.
@@ -852,7 +838,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                 if (!ok) break;
                 tc_fence_after();
             }
-            tmem_st32(t_base + P_COL + sb * 64u + half * 32, pk);
+            tmem_st16x2_32<32>(t_base + P_COL + sb * 64u, pk);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(C::B_P_FULL + sb));
@@ -861,25 +847,20 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
         }
         if (!ok) break;
         // ---- epilogue: the owner of this tile stores it to the destination shard
-        // (one slot suffices: before a thread writes it again, both threads of the
-        // row have passed the next block's max exchange, i.e. read this value)
-        xsum[half * BLOCK_M + row] = l_run;
-        ok = pair_exchange();
-        if (!ok) break;
-        const float l_row = xsum[row] + xsum[BLOCK_M + row];
+        const float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
         Work w;
         get_work<CAUSAL, VARLEN>(a, vt, u_iter, w);   // the same piece of work as above (recomputed, not kept live)
-        const int b = w.b, h = w.h, qt = w.qt;
+        const int b = w.b, h = a.h0_out + w.h, qt = w.qt;   // h: head in the output layout
         ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns, u_iter);
         if (!ok) break;
         tc_fence_after();
         if (w.kind == WORK_FULL) {
-            // Each lane holds one row; stores straight from the lanes would scatter
-            // 32 rows per instruction.  A 2 KB per-warp stage (32 rows x 64 B,
-            // 16-byte chunks XOR-swizzled against bank conflicts) lets 4 lanes write
-            // 64 contiguous bytes of a row: each store instruction covers 8 rows.
+            // Each lane holds half a row; stores straight from the lanes would
+            // scatter 32 pieces per instruction.  A 2 KB per-warp stage (32 half
+            // rows x 64 B, 16-byte chunks XOR-swizzled against bank conflicts) lets
+            // 4 lanes write 64 contiguous bytes: each store instruction covers 8 pieces.
             const int s_loc = qt * BLOCK_M + row;   // row within the sequence
-            unsigned long long dst_row = 0;   // this lane's row in the destination (0: past the sequence)
+            unsigned long long dst_row = 0;   // this lane's half row in the destination (0: past the sequence)
             if (s_loc < (VARLEN ? w.len : a.S)) {
                 const int s_row = (VARLEN ? w.row0 : 0) + s_loc;
                 const int p = s_row / a.epi.Sl + h / a.epi.Hl;
@@ -893,12 +874,11 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                     report_error(XS_DEVICE_BOUNDS_CODE, 2, p, s_row, h);
             }
             uint4* stage = reinterpret_cast<uint4*>(smem + C::STAGE_OFF + warp * 2048);
-            const int lane = static_cast<int>(lane_id());
             const float inv_l = 1.0f / l_row;
 #pragma unroll
             for (int q = 0; q < DH / 32; ++q) {
                 uint32_t orr[32];
-                tmem_ld32(t_base + O_COL + half * DH + q * 32, orr);
+                tmem_ld16x2_32<DH>(t_base + O_COL + q * 32, orr);
                 tmem_wait_ld();
                 uint32_t wv[16];
 #pragma unroll
@@ -911,7 +891,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                 __syncwarp();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int r = k * 8 + (lane >> 2);   // row (lane of the warp) this lane stores a chunk of
+                    const int r = k * 8 + (lane >> 2);   // lane whose half row this lane stores a chunk of
                     const int c4 = lane & 3;
                     const uint4 v = stage[r * 4 + (c4 ^ (r & 3))];
                     const unsigned long long rp = __shfl_sync(0xffffffffu, dst_row, r);
@@ -921,7 +901,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                 __syncwarp();   // the stage is rewritten by the next chunk
             }
         } else {
-            ok = split_epilogue<D>(a, w, t_base + O_COL + half * DH, row, half, warp, m_run, l_row,
+            ok = split_epilogue<D>(a, w, t_base + O_COL, row, half, warp, m_run, l_row,
                                    *reinterpret_cast<const volatile unsigned*>(smem + C::MISC_OFF + 8), abort_flag);
             if (!ok) break;
         }
@@ -956,7 +936,6 @@ __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorM
         mbar_init(bar0 + 8 * C::B_O_FINAL, 1);
         mbar_init(bar0 + 8 * C::B_O_FREE, NUM_SOFTMAX_WARPS);
         mbar_init(bar0 + 8 * C::B_DRAIN, 2);
-        for (int q = 0; q < 4; ++q) mbar_init(bar0 + 8 * (C::B_PAIR + q), 2);
         for (int s = 0; s < C::KV_STAGES; ++s) {
             mbar_init(bar0 + 8 * (C::B_KV_FULL + s), 1);
             mbar_init(bar0 + 8 * (C::B_KV_FREE + s), 1);

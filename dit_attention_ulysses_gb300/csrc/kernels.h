@@ -75,6 +75,10 @@ struct AttnArgs {
     int causal_head_major;  // causal tile order: 0 longest first with the B*H tiles of one
                             // query tile side by side; 1 head-major (a head's query tiles
                             // side by side, longest first within the head)
+    int h0;         // the launch's head h is head h0 + h of the input tensor maps ...
+    int h0_out;     // ... and head h0_out + h of the output layout (both 0: all heads;
+                    // a head group of larger tensors: both the group's first head; a
+                    // Ulysses rank r with H/P local heads: 0 and r * H/P)
 };
 
 // Packed variable-length sequences (B = 1, S = T rows in total): the sequence

@@ -163,6 +163,39 @@ int xs_attn_ulysses_fwd(const void* const* q_shards, const void* const* k_shards
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * xs_attn_ulysses_rank_fwd -- the attention of ONE Ulysses rank with the
+ * post-attention All-to-All fused into its epilogue, in the form a multi-GPU
+ * deployment runs (X-Stage, abstract; gist.science technical summary, "Key
+ * Contributions" item 3: the output-tile owner stores each finished tile to the
+ * rank that owns the tile's sequence block and resumes its next tile).  Rank
+ * `rank` of P holds, after the pre-attention exchange, all S rows of its H/P
+ * heads; it computes exact attention over them and stores each output row
+ * (b, s, j) straight into out_shards[s / (S/P)] at row (b, s % (S/P)) and global
+ * head rank * H/P + j.  Called once per rank with every rank's pointers, the P
+ * calls together fill the P sequence shards exactly as xs_attn_a2a_fwd does on
+ * the whole tensors (bit for bit without a workspace).
+ *   q_heads, k_heads, v_heads  device bf16 [B, S, H/P, D]: this rank's heads.
+ *   out_shards  host array of P device pointers, out_shards[p] = rank p's
+ *               sequence shard [B, S/P, H, D] (bf16).  Pointers into another
+ *               process's memory (CUDA IPC) or a peer GPU's are plain
+ *               addresses to the kernel: its 16-byte stores go there directly.
+ *               The call only writes the rows of heads [rank*H/P, (rank+1)*H/P).
+ *   B, S, H, D  global shape (H = total heads, H % P == 0, S % P == 0).
+ *   rank        0 .. P-1.
+ *   workspace, workspace_bytes  as in xs_attn_fwd_balanced, sized for H/P heads
+ *               (xs_attn_workspace_bytes(B, S, H/P, D)); NULL, 0: whole tiles.
+ * Completion: the stores are visible to the owners of the shards once `stream`
+ * has passed the call (for other processes: after an event recorded there);
+ * the library adds no flag or barrier of its own.
+ * Returns XS_OK or XS_ERR_NULL / _SHAPE (rank out of range) / _HEAD_DIM /
+ * _DIVISIBILITY / _TOO_MANY_RANKS / _ALIGNMENT / _OVERLAP / _SCALE /
+ * _WORKSPACE / _CUDA.
+ */
+int xs_attn_ulysses_rank_fwd(const void* q_heads, const void* k_heads, const void* v_heads,
+                             void* const* out_shards, int B, int S, int H, int D, int P, int rank,
+                             float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * xs_relayout_a2a_inverse -- the separate pre-attention All-to-All re-layout
  * (single GPU), the inverse of xs_relayout_a2a:
  *     heads[r][b, s, j, :] = seq_shards[s / (S/P)][b, s % (S/P), r*(H/P) + j, :]
@@ -177,13 +210,25 @@ int xs_relayout_a2a_inverse(const void* const* seq_shards, void* const* heads,
 
 /*
  * xs_attn_a2a_fwd_staged -- xs_attn_a2a_fwd for host-resident data.
- * Copies q, k, v from host memory (pinned for asynchronous copies) into the
- * caller's device buffers q_dev, k_dev, v_dev, runs the fused kernel into the
- * caller's device shards out_dev[p], and copies every shard back into the host
- * buffers out_host[p]; all on `stream`, in that order.  The host buffers must
- * stay alive and untouched until the stream has finished.  Device-side rules
- * are those of xs_attn_a2a_fwd; workspace / workspace_bytes are those of
- * xs_attn_fwd_balanced (NULL, 0: the plain schedule).
+ * Copies q, k, v from host memory into the caller's device buffers q_dev,
+ * k_dev, v_dev, runs the fused kernel into the caller's device shards
+ * out_dev[p], and copies every shard back into the host buffers out_host[p].
+ * The work is pipelined over min(H, 8) groups of heads: the kernel of group g
+ * runs on `stream` while the host-to-device copies of group g + 1 run on one
+ * library stream and the device-to-host copies of group g - 1 on another (one
+ * pitched cudaMemcpy2DAsync per tensor and group: a group's heads are a
+ * contiguous run of every [.., H, D] row).  Each group's launch computes only its
+ * heads (the schedule planned for them; the workspace is used when it is large
+ * enough for the group's plan, else whole tiles run); the results are those of
+ * xs_attn_a2a_fwd.  `stream` waits for the last copy before the call's end, and
+ * the copies wait for the work queued on `stream` before the call, so the call
+ * is ordered on `stream` like any other.  Host buffers should be pinned (page-
+ * locked); otherwise the copies do not overlap.  They must stay alive and
+ * untouched until the stream has finished.  The library keeps two streams and
+ * 18 events per device for this (created at the first call, kept until exit);
+ * calls from several host threads are enqueued one at a time.  Device-side
+ * rules are those of xs_attn_a2a_fwd; workspace / workspace_bytes those of
+ * xs_attn_fwd_balanced (NULL, 0: whole tiles).
  */
 int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v_host,
                            void* const* out_host,

@@ -32,29 +32,7 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-MIN_PIECE = 8   # key blocks per CTA range, at least
-MIN_GAIN = 16   # key blocks a split must save per CTA, at least
-
-
-def split_tiles(tiles, n, G):
-    """{tile: [cut blocks]} of the balanced schedule: whole waves run whole; the
-    key blocks of the tiles % G leftover tiles are cut into C = min(G, rem*n // 8)
-    equal ranges (range i starts at iteration rem*n*i // C), used only if C > rem
-    and a range is shorter than a tile by at least max(16, n // 8) blocks."""
-    rem = tiles % G
-    if rem == 0:
-        return {}
-    sk = rem * n
-    ctas = min(G, sk // MIN_PIECE)
-    if ctas <= rem or n - (sk + ctas - 1) // ctas < max(MIN_GAIN, n // 8):
-        return {}
-    dp = tiles - rem
-    out = {}
-    for i in range(1, ctas):
-        start = sk * i // ctas
-        if start % n:
-            out.setdefault(dp + start // n, []).append(start % n)
-    return out
+from _schedule import split_tiles  # noqa: E402
 
 
 # (S, D, P, B, H) on 152 SMs: tiles cut in four (S=4096, H=5), in two or three
@@ -239,9 +217,13 @@ def test_balanced_expired_wait_is_reported(xs, monkeypatch):
     assert_close(np.stack([torch_to_f64(o) for o in outs]), ref, mass, "balanced after timeout")
 
 
-def test_staged_host_entry_with_workspace_matches_device_entry(xs):
-    """xs_attn_a2a_fwd_staged with a workspace (H2D, balanced kernel, D2H on one
-    stream) returns exactly the shards of the device-side balanced call."""
+def test_staged_host_entry_with_workspace_vs_oracle(xs):
+    """xs_attn_a2a_fwd_staged with a workspace: the head groups of its pipeline
+    run the balanced schedule planned for their own heads (here every one-head
+    group splits its 32 tiles over 128 CTAs), so its split tiles are merged in a
+    different order than the whole-shape call's: checked against the oracle and
+    against the device-side call to rounding."""
+    import oracle
     S, D, P, B, H = SHAPES[0]
     _check_splits(B, S, H)
     ws = xs.Workspace(xs.xs_attn_workspace_bytes(B, S, H, D))
@@ -256,8 +238,11 @@ def test_staged_host_entry_with_workspace_matches_device_entry(xs):
     xs.xs_attn_a2a_fwd_staged(qh, kh, vh, out_h, qd, kd, vd, out_d, w.scale, workspace=ws)
     torch.cuda.synchronize()
     assert xs.xs_attn_get_device_error() == xs.XS_OK
-    for a, b in zip(out_h, ref):
-        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
+    got = np.stack([torch_to_f64(o) for o in out_h])
+    exp = oracle.attention_a2a(*bits, w.scale, P)
+    mass = oracle.attention_a2a(bits[0], bits[1], abs_bits(bits[2]), w.scale, P)
+    assert_close(got, exp, mass, "staged with a workspace")
+    assert max(float((a.float() - b.cpu().float()).abs().max()) for a, b in zip(out_h, ref)) <= 2e-2
 
 
 def test_balanced_graph_replay_takes_only_its_own_flags(xs):

@@ -173,19 +173,32 @@ def test_deterministic(xs):
 
 
 def test_staged_host_entry_matches_device_entry(xs):
-    w = di.Workload("st", B=1, H=4, S=1024, D=128, P=4, scale=1 / math.sqrt(128))
-    qb, kb, vb = di.random_qkv(w)
-    dev = _run_fused(xs, qb, kb, vb, w.scale, 4)
+    """The host-buffer entry pipelines min(H, 8) head groups (copies of the next
+    group in, kernel of this one, copies of the last one out, on three streams);
+    without a workspace every group runs whole tiles, whose arithmetic is the
+    whole-tensor kernel's, so the shards agree bit for bit.  Two calls back to
+    back on a side stream, on the same device buffers with different host
+    inputs: the second call's copies must wait for the first call's kernels."""
+    w1 = di.Workload("st", B=1, H=12, S=1024, D=128, P=4, scale=1 / math.sqrt(128))
+    w2 = di.Workload("st2", B=1, H=12, S=1024, D=128, P=4, scale=1 / math.sqrt(128), seed=9)
     pin = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
-    qh, kh, vh = pin(qb), pin(kb), pin(vb)
-    shape = (1, 256, 4, 128)
-    out_h = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(4)]
-    qd, kd, vd = (torch.empty_like(x, device="cuda") for x in (qh, kh, vh))
+    shape = (1, 256, 12, 128)
+    qd, kd, vd = (torch.empty((1, 1024, 12, 128), dtype=torch.bfloat16, device="cuda") for _ in range(3))
     out_d = [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
-    xs.xs_attn_a2a_fwd_staged(qh, kh, vh, out_h, qd, kd, vd, out_d, w.scale)
-    torch.cuda.synchronize()
-    for a, b in zip(dev, out_h):
-        assert torch.equal(a.cpu().view(torch.int16), b.view(torch.int16))
+    side = torch.cuda.Stream()
+    outs, devs, keep = [], [], []
+    for w in (w1, w2):
+        qb, kb, vb = di.random_qkv(w)
+        devs.append(_run_fused(xs, qb, kb, vb, w.scale, 4))
+        out_h = [torch.full(shape, float("nan"), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+        keep.append([pin(x) for x in (qb, kb, vb)])   # host inputs live until the stream is done
+        xs.xs_attn_a2a_fwd_staged(*keep[-1], out_h, qd, kd, vd, out_d, w.scale, stream=side)
+        outs.append(out_h)
+    side.synchronize()
+    assert xs.xs_attn_get_device_error(side) == xs.XS_OK
+    for dev, out_h in zip(devs, outs):
+        for a, b in zip(dev, out_h):
+            assert torch.equal(a.cpu().view(torch.int16), b.view(torch.int16))
 
 
 def test_non_default_stream(xs):

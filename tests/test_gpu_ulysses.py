@@ -169,3 +169,72 @@ def test_ulysses_rejects_tiles_straddling_shards(xs):
     with pytest.raises(xs.XsError) as e:
         xs.xs_attn_ulysses_fwd(q, q, q, outs, 0.1)
     assert e.value.code == xs.XS_ERR_DIVISIBILITY
+
+
+# ---- one rank's attention with the post-attention exchange in its epilogue
+RANK_CASES = [
+    # B, S, H, D, P
+    (1, 1024, 8, 128, 4),
+    (2, 1000, 4, 64, 2),      # shards of 500 rows: tiles straddle shard boundaries
+    (1, 4608, 24, 128, 4),    # the image-DiT shape
+]
+
+
+def _rank_calls(xs, q, k, v, P, scale, ws=None):
+    """P calls of xs_attn_ulysses_rank_fwd, rank r on heads [r*H/P, (r+1)*H/P)."""
+    B, S, H, D = q.shape
+    Hl = H // P
+    outs = _shards_like(B, S, H, D, P)
+    for r in range(P):
+        sl = slice(r * Hl, (r + 1) * Hl)
+        xs.xs_attn_ulysses_rank_fwd(q[:, :, sl].contiguous(), k[:, :, sl].contiguous(), v[:, :, sl].contiguous(),
+                                    outs, H, r, scale, ws)
+    torch.cuda.synchronize()
+    assert xs.xs_attn_get_device_error() == xs.XS_OK
+    return outs
+
+
+@pytest.mark.parametrize("B,S,H,D,P", RANK_CASES, ids=[f"B{c[0]}_S{c[1]}_H{c[2]}_D{c[3]}_P{c[4]}" for c in RANK_CASES])
+def test_rank_entry_fills_shards_like_fused_kernel(xs, B, S, H, D, P):
+    """Every rank stores its heads' rows into all P shards at head offset r*H/P;
+    together the P calls give the fused kernel's shards bit for bit (a head's
+    tiles do the same arithmetic whatever other heads the launch holds)."""
+    w = di.Workload("rank", B=B, H=H, S=S, D=D, P=P, scale=1 / math.sqrt(D), seed=S + H)
+    q, k, v = (bits_to_torch(x) for x in di.random_qkv(w))
+    got = _rank_calls(xs, q, k, v, P, w.scale)
+    ref = _shards_like(B, S, H, D, P)
+    xs.xs_attn_a2a_fwd(q, k, v, ref, w.scale)
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_rank_entry_layout_code_and_balanced_vs_oracle(xs):
+    """Index-coded inputs: every output row is its own V row at its global head;
+    and random inputs with the balanced schedule (workspace sized for H/P heads)
+    against the oracle's whole path."""
+    import oracle
+    B, S, H, D, P = 1, 4096, 10, 128, 2
+    q, k, v, scale = di.layout_code_inputs_torch(B, S, H, D)
+    outs = _rank_calls(xs, q, k, v, P, scale)
+    Sl = S // P
+    for p in range(P):
+        exp = di.layout_code_value_torch(B, S, H, D, s_offset=p * Sl, S_rows=Sl)
+        assert torch.equal(outs[p].view(torch.int16), exp.view(torch.int16)), f"shard {p}"
+    w = di.Workload("rankbal", B=B, H=H, S=S, D=D, P=P, scale=1 / math.sqrt(D), seed=5)
+    qb, kb, vb = di.random_qkv(w)
+    need = xs.xs_attn_workspace_bytes(B, S, H // P, D)
+    assert need > 0, "5 heads of 32 tiles leave 8 tiles to split on 152 SMs"
+    ws = xs.Workspace(need)
+    outs = _rank_calls(xs, *(bits_to_torch(x) for x in (qb, kb, vb)), P, w.scale, ws)
+    ref = oracle.attention_a2a(qb, kb, vb, w.scale, P)
+    mass = oracle.attention_a2a(qb, kb, abs_bits(vb), w.scale, P)
+    assert_close(np.stack([torch_to_f64(o) for o in outs]), ref, mass, "rank entry, balanced")
+
+
+def test_rank_entry_rejects_bad_rank(xs):
+    q = torch.zeros((1, 256, 1, 64), dtype=torch.bfloat16, device="cuda")
+    outs = _shards_like(1, 256, 2, 64, 2)
+    with pytest.raises(xs.XsError) as e:
+        xs.xs_attn_ulysses_rank_fwd(q, q, q, outs, 2, 2, 0.1)
+    assert e.value.code == xs.XS_ERR_SHAPE
