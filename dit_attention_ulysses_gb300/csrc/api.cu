@@ -340,7 +340,15 @@ int run_attention(const void* q, const void* k, const void* v, const void* const
             if ((rc = encode_bshd(&maps.v[p], shards[2 * P + p], B, Sl, H, D)) != XS_OK) return rc;
         }
         a.in_Sl = Sl;
-        a.in_inv_Sl = 1.0f / static_cast<float>(Sl);
+        // shard of key block x (< 2^16): floor(x / bps) = umulhi(2x, m) >> k with
+        // k = floor(log2 bps) and m = ceil(2^(31 + k) / bps) < 2^32: the error of
+        // m is below x / 2^31 < 2^-15 after the shift, below the 2^k / bps >= 1/2
+        // gap to the next multiple
+        const unsigned bps = static_cast<unsigned>(Sl / 128);
+        int k = 0;
+        while ((2u << k) <= bps) ++k;
+        a.in_magic = static_cast<unsigned>(((1ull << (31 + k)) + bps - 1) / bps);
+        a.in_shift = k;
         e = (D == 128) ? xs::launch_attn_sharded<128>(maps, P, a, grid, split, stream)
                        : xs::launch_attn_sharded<64>(maps, P, a, grid, split, stream);
     } else {
@@ -682,6 +690,7 @@ int xs_attn_ulysses_fwd(const void* const* q_shards, const void* const* k_shards
     if (rc != XS_OK) return rc;
     const int Sl = S / P;
     if (Sl % 128 != 0) return XS_ERR_DIVISIBILITY;
+    if ((S + 127) / 128 > 65536) return XS_ERR_SHAPE;   // the kernel's shard lookup covers 2^16 key blocks
     const void* in[3 * XS_MAX_P];
     for (int p = 0; p < P; ++p) {
         in[p] = q_shards[p];

@@ -71,7 +71,8 @@ struct AttnArgs {
     SplitParams sp;
     int in_Sl;      // inputs as sequence shards: rows per shard (a multiple of 128);
                     // 0: one [B, S, H, D] tensor per operand
-    float in_inv_Sl;  // 1 / in_Sl (fp32), for a division-free shard lookup
+    unsigned in_magic;  // shard lookup without division: shard = umulhi(2 * (row / 128), in_magic)
+    int in_shift;       //   >> in_shift (see pick_map); set with in_Sl
     int causal_head_major;  // causal tile order: 0 longest first with the B*H tiles of one
                             // query tile side by side; 1 head-major (a head's query tiles
                             // side by side, longest first within the head)
