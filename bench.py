@@ -568,6 +568,35 @@ def run_sweep(args):
                       "kernel_source": kernel_source_hash()}), flush=True)
 
 
+def run_tile_spans(args):
+    """One launch of the instrumented build (per-tile timestamps) on the workload:
+    block period, PV tail, epilogue (the fused stores) and refill per tile."""
+    import torch
+
+    import dit_attention_ulysses_gb300 as xs
+    from dit_attention_ulysses_gb300 import spans
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = di.WORKLOADS[args.workload]
+    q, k, v = (to_device(x, torch, dev) for x in di.random_qkv(w))
+    outs = [torch.empty((w.B, w.S // w.P, w.H, w.D), dtype=torch.bfloat16, device=dev) for _ in range(w.P)]
+    ws = xs.Workspace.for_shape(w.B, w.S, w.H, w.D, device=dev) if args.schedule == "balanced" else None
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    per_cta = -(-w.B * w.H * ((w.S + 127) // 128) // sms) + 2
+    for _ in range(3):   # warm-up of the instrumented library, then the recorded launch
+        st = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
+    sampler = ClockSampler(0)
+    sampler.start()
+    t0 = time.time()
+    st = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
+    clocks = sampler.stop(t0, time.time())
+    ghz = (clocks.get("sm_mhz") or 2070.0) / 1e3
+    summary = spans.summarize(st, ghz)
+    print(json.dumps({"tile_spans": summary, "workload": w.name, "sm_ghz_assumed": ghz, "clocks": clocks,
+                      "kernel_source": kernel_source_hash()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -581,6 +610,8 @@ def main():
                          "plain: whole tiles only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--tile-spans", action="store_true",
+                    help="record one launch of the per-tile timestamp build on --workload and print its spans")
     ap.add_argument("--sweep", action="store_true",
                     help="time the sequence sweep (fused, attention alone, attention + re-layout at every S) "
                          "and print it as one JSON record instead of the benchmark line")
@@ -594,6 +625,10 @@ def main():
     if args.sweep:
         if rank == 0:
             run_sweep(args)
+        return
+    if args.tile_spans:
+        if rank == 0:
+            run_tile_spans(args)
         return
     if world > 1:
         import torch.distributed as dist

@@ -13,7 +13,6 @@ from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
-LIB = os.path.join(HERE, "libxsattn.so")
 SOURCES = ["attn_fwd.cu", "relayout.cu", "burst_gap.cu", "api.cu"]
 HEADERS = ["kernels.h", "ptx.cuh", os.path.join("..", "..", "include", "xsattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -33,21 +32,32 @@ def _nvcc() -> str:
     return os.path.join(cuda_home(), "bin", "nvcc")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+# Library variants: the product library, and a build with per-tile timestamps
+# (XS_TILE_SPANS; read by dit_attention_ulysses_gb300.spans) for measurements.
+VARIANTS = {"": ([], "libxsattn.so", "_build"), "spans": (["-DXS_TILE_SPANS"], "libxsattn_spans.so", "_build_spans")}
+
+
+def lib_path(variant: str = "") -> str:
+    return os.path.join(HERE, VARIANTS[variant][1])
+
+
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, s) for s in SOURCES + HEADERS] + [__file__]
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of libxsattn.so."""
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
+    """Compile (if stale) and return the path of libxsattn.so (or of a variant)."""
+    defines, lib_name, build_dir = VARIANTS[variant]
+    LIB = os.path.join(HERE, lib_name)
+    if not force and not _stale(LIB):
         return LIB
-    bdir = os.path.join(HERE, "_build")
+    bdir = os.path.join(HERE, build_dir)
     os.makedirs(bdir, exist_ok=True)
-    flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I", CSRC]
+    flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I", CSRC] + defines
     if verbose:
         flags += ["-Xptxas", "-v"]
 
@@ -78,4 +88,4 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 if __name__ == "__main__":
     import sys
-    print(build(force=True, verbose="-v" in sys.argv))
+    print(build(force=True, verbose="-v" in sys.argv, variant="spans" if "spans" in sys.argv else ""))

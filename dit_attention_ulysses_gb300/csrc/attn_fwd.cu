@@ -74,6 +74,29 @@ __device__ int g_device_error = 0;
 __device__ DeviceErrorInfo g_error_info;
 __device__ int g_drain_failed = 0;
 
+// Per-tile timestamps (a build with XS_TILE_SPANS only; the library's normal
+// build compiles the stamps to nothing).  Warp 0, lane 0 of the softmax records,
+// for the k-th piece of work of its CTA, SPAN_WORDS words at
+// g_spans[(cta * g_spans_per_cta + k) * SPAN_WORDS]:
+//   0 %globaltimer when the piece's first scores are seen   1 clock64 then
+//   2 clock64 when the piece's last P is written            3 clock64 when its last PV is done
+//   4 clock64 after the epilogue's stores are issued        5 (key blocks << 32) | piece kind
+// (clock64 is the SM's cycle counter: differences within one CTA are cycles).
+#ifdef XS_TILE_SPANS
+constexpr int SPAN_WORDS = 6;
+__device__ unsigned long long* g_spans = nullptr;
+__device__ int g_spans_per_cta = 0;
+__device__ __forceinline__ void span_stamp(int k, int slot, unsigned long long v) {
+    unsigned long long* s = g_spans;
+    if (s != nullptr && k < g_spans_per_cta && threadIdx.x == 0)
+        s[(static_cast<size_t>(blockIdx.x) * g_spans_per_cta + k) * SPAN_WORDS + slot] = v;
+}
+__device__ __forceinline__ unsigned long long span_clock() { return static_cast<unsigned long long>(clock64()); }
+#else
+__device__ __forceinline__ void span_stamp(int, int, unsigned long long) {}
+__device__ __forceinline__ unsigned long long span_clock() { return 0; }
+#endif
+
 // Records the first device error of the launch (later ones only find the word
 // set).  Out of line: it runs at most once per launch and must not weigh on the
 // register allocation of the loops that call it.
@@ -506,6 +529,9 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
         const int qb = u_iter % C::Q_BUFS;
         const uint64_t qdesc = desc_add(qdesc0, qb * (C::TILE_BYTES >> 4));
         ok = thread_wait(bar(C::B_Q_FULL + qb), (u_iter / C::Q_BUFS) & 1, abort_flag, a.timeout_ns, u_iter);
+        // the previous piece's last PV first: its epilogue waits for it, while
+        // this piece's first scores are only read after that epilogue
+        if (ok && u_iter > 0) ok = thread_wait(bar(C::B_O_FINAL), (u_iter - 1) & 1, abort_flag, a.timeout_ns, u_iter);
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gs = g + j;
             const uint32_t sb = gs & 1;
@@ -789,6 +815,10 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             const uint32_t sb = g & 1;
             ok = warp_wait(bar(C::B_S_FULL + sb), (g >> 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
             if (!ok) break;
+            if (j == 0) {
+                span_stamp(u_iter, 0, globaltimer_ns());
+                span_stamp(u_iter, 1, span_clock());
+            }
             tc_fence_after();
             uint32_t sr[2][32];
             tmem_ld16x2_32<64>(t_base + S_COL + sb * 128u, sr[0]);
@@ -853,6 +883,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(C::B_P_FULL + sb));
+            if (j == n - 1) span_stamp(u_iter, 2, span_clock());
             l_run = l_run * alpha + sum;
             m_run = m_use;
         }
@@ -864,6 +895,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
         const int b = w.b, h = a.h0_out + w.h, qt = w.qt;   // h: head in the output layout
         ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns, u_iter);
         if (!ok) break;
+        span_stamp(u_iter, 3, span_clock());
         tc_fence_after();
         if (w.kind == WORK_FULL) {
             // Each lane holds half a row; stores straight from the lanes would
@@ -916,6 +948,8 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                                    *reinterpret_cast<const volatile unsigned*>(smem + C::MISC_OFF + 8), abort_flag);
             if (!ok) break;
         }
+        span_stamp(u_iter, 4, span_clock());
+        span_stamp(u_iter, 5, (static_cast<unsigned long long>(w.nb) << 32) | static_cast<unsigned>(w.kind));
         tc_fence_before();
         warp_arrive(bar(C::B_O_FREE));
         ++u_iter;
@@ -1126,6 +1160,14 @@ template cudaError_t launch_attn<64>(const CUtensorMap&, const CUtensorMap&, con
                                      bool, cudaStream_t);
 template cudaError_t launch_attn<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const AttnArgs&,
                                       int, bool, cudaStream_t);
+
+#ifdef XS_TILE_SPANS
+cudaError_t set_tile_spans(unsigned long long* buf, int per_cta) {
+    cudaError_t e = cudaMemcpyToSymbol(g_spans, &buf, sizeof buf);
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_spans_per_cta, &per_cta, sizeof per_cta);
+}
+#endif
 
 cudaError_t read_and_clear_device_error(int* value, DeviceErrorInfo* info, int* drain_failed) {
     int zero = 0;

@@ -134,6 +134,12 @@ cudaError_t launch_attn_sharded(const ShardMaps& maps, int P, const AttnArgs& ar
 // a CTA exited).
 cudaError_t read_and_clear_device_error(int* value, DeviceErrorInfo* info, int* drain_failed);
 
+#ifdef XS_TILE_SPANS
+// Instrumented build only: where the per-tile timestamps go (device buffer of
+// grid * per_cta * 6 words; NULL stops recording).
+cudaError_t set_tile_spans(unsigned long long* buf, int per_cta);
+#endif
+
 struct RelayoutArgs {
     const void* heads[MAX_PTRS];
     void* out[MAX_PTRS];

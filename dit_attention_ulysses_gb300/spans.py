@@ -1,0 +1,112 @@
+"""Per-tile timestamps of the attention kernel: where a tile's time goes.
+
+X-Stage (gist.science technical summary, "Results") reads the fused kernel's
+behaviour from per-tile store spans.  This module runs the attention kernel from
+a separately built library, ``libxsattn_spans.so`` (the same sources compiled
+with ``XS_TILE_SPANS``; the product library has no stamps), in which warp 0 of
+every CTA records six words per piece of work:
+
+  0  %globaltimer (ns) when the piece's first scores are seen
+  1  clock64 at the same moment
+  2  clock64 when the piece's last P is written to tensor memory
+  3  clock64 when its last PV has completed (the epilogue may start)
+  4  clock64 after the epilogue's stores to the owner's shard are issued
+  5  (key blocks << 32) | piece kind (0 whole tile, 1 head of a split tile, 2 part)
+
+``summarize`` turns a recording into per-tile spans in SM cycles and
+microseconds: the block period (first scores to last P, per key block), the PV
+tail (last P to last PV done), the epilogue span (last PV done to stores
+issued: the fused All-to-All's cost on the critical path) and the refill (stores
+issued to the next piece's first scores in the same CTA).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+SPAN_WORDS = 6
+
+
+def parse(stamps: np.ndarray) -> list[dict]:
+    """Recorded words [grid, per_cta, 6] (uint64) -> one dict per recorded piece, in
+    CTA order and piece order, with the raw stamps, the CTA and the piece index."""
+    stamps = np.asarray(stamps, dtype=np.uint64)
+    out = []
+    for cta in range(stamps.shape[0]):
+        for k in range(stamps.shape[1]):
+            w = [int(x) for x in stamps[cta, k]]
+            if w[5] == 0:
+                continue
+            out.append({"cta": cta, "piece": k, "blocks": w[5] >> 32, "kind": w[5] & 0xFFFFFFFF,
+                        "t_ns": w[0], "c_first": w[1], "c_last_p": w[2], "c_o_done": w[3], "c_stored": w[4]})
+    return out
+
+
+def _stats(x):
+    x = np.asarray(x, dtype=np.float64)
+    if x.size == 0:
+        return None
+    p10, p50, p90 = np.percentile(x, [10, 50, 90])
+    return {"p10": float(p10), "p50": float(p50), "p90": float(p90), "n": int(x.size)}
+
+
+def summarize(stamps: np.ndarray, sm_ghz: float) -> dict:
+    """Spans of every recorded piece (cycles, and microseconds at sm_ghz):
+    block period, PV tail, epilogue (store) span and refill, as p10/p50/p90."""
+    recs = parse(stamps)
+    per_block, tail, epi, refill = [], [], [], []
+    by_cta = {}
+    for r in recs:
+        by_cta.setdefault(r["cta"], []).append(r)
+        if r["blocks"] > 1:
+            per_block.append((r["c_last_p"] - r["c_first"]) / (r["blocks"] - 1))
+        tail.append(r["c_o_done"] - r["c_last_p"])
+        epi.append(r["c_stored"] - r["c_o_done"])
+    for rs in by_cta.values():
+        rs.sort(key=lambda r: r["piece"])
+        for a, b in zip(rs, rs[1:]):
+            if b["piece"] == a["piece"] + 1:
+                refill.append(b["c_first"] - a["c_stored"])
+    to_us = lambda s: None if s is None else {k: (v / (sm_ghz * 1e3) if k != "n" else v) for k, v in s.items()}
+    cyc = {"block_period": _stats(per_block), "pv_tail": _stats(tail), "epilogue": _stats(epi),
+           "refill": _stats(refill)}
+    starts = [r["t_ns"] for r in recs]
+    return {"pieces": len(recs), "ctas": len(by_cta), "cycles": cyc, "us": {k: to_us(v) for k, v in cyc.items()},
+            "first_to_last_start_us": (max(starts) - min(starts)) / 1e3 if starts else None}
+
+
+def load():
+    """The instrumented library (built here if needed), with the entry points used."""
+    from . import _build
+    path = _build.build(variant="spans")
+    lib = ctypes.CDLL(path)
+    lib.xs_attn_set_tile_spans.restype = ctypes.c_int
+    lib.xs_attn_set_tile_spans.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.xs_attn_fwd_balanced.restype = ctypes.c_int
+    lib.xs_attn_fwd_balanced.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p)] + \
+        [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.xs_attn_get_device_error.restype = ctypes.c_int
+    lib.xs_attn_get_device_error.argtypes = [ctypes.c_void_p]
+    return lib
+
+
+def record(q, k, v, outs, layout: int, scale: float, per_cta: int, workspace=None):
+    """One launch of the instrumented kernel (xs_attn_fwd_balanced's arguments, torch
+    tensors on the current device); returns the stamps [grid, per_cta, 6] as uint64."""
+    import torch
+    lib = load()
+    sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+    buf = torch.zeros((sms, per_cta, SPAN_WORDS), dtype=torch.int64, device=q.device)
+    if lib.xs_attn_set_tile_spans(buf.data_ptr(), per_cta) != 0:
+        raise RuntimeError("xs_attn_set_tile_spans failed")
+    B, S, H, D = q.shape
+    ptrs = (ctypes.c_void_p * len(outs))(*[o.data_ptr() for o in outs])
+    wp, wn = (workspace.ptr, workspace.nbytes) if workspace is not None else (None, 0)
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = lib.xs_attn_fwd_balanced(q.data_ptr(), k.data_ptr(), v.data_ptr(), layout, ptrs, B, S, H, D, len(outs),
+                                  scale, wp, wn, stream)
+    if rc != 0 or lib.xs_attn_get_device_error(stream) != 0:
+        raise RuntimeError(f"instrumented launch failed ({rc})")
+    lib.xs_attn_set_tile_spans(None, 0)
+    return buf.cpu().numpy().view(np.uint64)

@@ -1,0 +1,40 @@
+"""The per-tile timestamp reader (dit_attention_ulysses_gb300.spans) on a
+synthetic recording with known spans: every figure of the summary must come
+out as constructed."""
+import numpy as np
+
+from dit_attention_ulysses_gb300.spans import SPAN_WORDS, parse, summarize
+
+
+def _recording():
+    # 2 CTAs x 4 slots; CTA 0 records 3 pieces, CTA 1 records 2 (slot 2 empty);
+    # block period 1000 cycles, PV tail 700, epilogue 2000, refill 1500
+    st = np.zeros((2, 4, SPAN_WORDS), dtype=np.uint64)
+    for cta, pieces in ((0, 3), (1, 2)):
+        c = 10_000 * (cta + 1)
+        for k in range(pieces):
+            blocks = 36
+            first = c
+            last_p = first + 1000 * (blocks - 1)
+            o_done = last_p + 700
+            stored = o_done + 2000
+            st[cta, k] = [5_000_000 + 17 * k + 3 * cta, first, last_p, o_done, stored, (blocks << 32) | 0]
+            c = stored + 1500
+    return st
+
+
+def test_parse_skips_empty_slots_and_keeps_order():
+    recs = parse(_recording())
+    assert [(r["cta"], r["piece"]) for r in recs] == [(0, 0), (0, 1), (0, 2), (1, 0), (1, 1)]
+    assert all(r["blocks"] == 36 and r["kind"] == 0 for r in recs)
+
+
+def test_summary_recovers_the_constructed_spans():
+    s = summarize(_recording(), sm_ghz=2.0)
+    assert s["pieces"] == 5 and s["ctas"] == 2
+    c = s["cycles"]
+    assert c["block_period"]["p50"] == 1000 and c["pv_tail"]["p50"] == 700
+    assert c["epilogue"]["p10"] == c["epilogue"]["p90"] == 2000
+    assert c["refill"]["n"] == 3 and c["refill"]["p50"] == 1500       # 2 in CTA 0, 1 in CTA 1
+    assert abs(s["us"]["epilogue"]["p50"] - 1.0) < 1e-12                 # 2000 cycles at 2 GHz
+    assert s["first_to_last_start_us"] == (17 * 2) / 1e3                 # ns -> us
