@@ -446,7 +446,8 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(2):
         e2e_fn()
     n_e2e = max(3, min(args.steps, 20))
-    e2e_ms = max_over_ranks(statistics.mean(time_steps(torch, e2e_fn, n_e2e, flush, stream)), world)
+    e2e_steps = time_steps(torch, e2e_fn, n_e2e, flush, stream)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_steps), world)
     if xs.xs_attn_get_device_error(stream) != 0:
         raise RuntimeError("device error after ablation / e2e runs")
     side = side_workload_line(torch, xs, args, dev, stream, flush) if args.workload != SIDE_WORKLOAD else None
@@ -487,7 +488,8 @@ def run_ours(args, rank, world, local_rank):
                      "order": "interleaved alone/fused/serial, L2 flushed before each"},
         "e2e": {"value": whole_job_tflops(w.flops, e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 3 * w.tensor_bytes, "d2h_bytes_per_step": w.tensor_bytes,
-                "ms_per_step": e2e_ms, "api": "xs_attn_a2a_fwd_staged"},
+                "ms_per_step": e2e_ms, "step_ms_percentiles": step_percentiles(e2e_steps),
+                "api": "xs_attn_a2a_fwd_staged"},
         "ulysses_step": ulysses,
         "causal": causal_line,
         "varlen": varlen_line,
@@ -585,15 +587,15 @@ def run_tile_spans(args):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     per_cta = -(-w.B * w.H * ((w.S + 127) // 128) // sms) + 2
     for _ in range(3):   # warm-up of the instrumented library, then the recorded launch
-        st = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
+        st, ph = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
     sampler = ClockSampler(0)
     sampler.start()
     t0 = time.time()
-    st = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
+    st, ph = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
     clocks = sampler.stop(t0, time.time())
     ghz = (clocks.get("sm_mhz") or 2070.0) / 1e3
-    summary = spans.summarize(st, ghz)
-    print(json.dumps({"tile_spans": summary, "workload": w.name, "sm_ghz_assumed": ghz, "clocks": clocks,
+    print(json.dumps({"tile_spans": spans.summarize(st, ghz), "block_phases_cycles": spans.summarize_phases(ph),
+                      "workload": w.name, "sm_ghz_assumed": ghz, "clocks": clocks,
                       "kernel_source": kernel_source_hash()}), flush=True)
 
 

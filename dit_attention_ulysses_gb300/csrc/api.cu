@@ -968,10 +968,11 @@ int xs_attn_last_cuda_error(void) { return g_last_cuda_error; }
 #ifdef XS_TILE_SPANS
 // Exported by the instrumented build only (libxsattn_spans.so), not declared in
 // the public header: point the kernels' per-tile timestamps at `buf` (device,
-// grid * per_cta * 6 unsigned 64-bit words), or stop with NULL.
-int xs_attn_set_tile_spans(void* buf, int per_cta) {
-    if (per_cta < 0 || (buf && per_cta == 0)) return XS_ERR_SHAPE;
-    const cudaError_t e = xs::set_tile_spans(static_cast<unsigned long long*>(buf), per_cta);
+// ctas * (per_cta * 6 + 32 * 10) unsigned 64-bit words: the per-piece words of
+// CTAs 0 .. ctas-1, then their block phases), or stop with NULL.
+int xs_attn_set_tile_spans(void* buf, int ctas, int per_cta) {
+    if (ctas < 0 || per_cta < 0 || (buf && (ctas == 0 || per_cta == 0))) return XS_ERR_SHAPE;
+    const cudaError_t e = xs::set_tile_spans(static_cast<unsigned long long*>(buf), ctas, per_cta);
     return e == cudaSuccess ? XS_OK : cuda_fail(e);
 }
 #endif

@@ -36,22 +36,22 @@
 // tensor map per shard: the pre-attention exchange fused into the loads).
 //
 // TMEM (512 columns x 128 lanes, fp32):
-//   [  0,128) S buffer 0    [128,256) S buffer 1        (scores, double-buffered)
-//   [256,320) P buffer 0    [320,384) P buffer 1        (bf16 P, 2 per column)
+//   [  0,128) S buffer 0    [128,256) S buffer 1    [256,384) S buffer 2
 //   [384,384+D) O accumulator
-// S(j+2) is issued as soon as the softmax has read S(j) (and K(j+2) has
-// arrived); PV(j) as soon as P(j) is written.  The tensor core computes S(j+2)
-// and PV(j) while the softmax works on block j+1, so softmax and MMAs overlap
-// completely; the softmax never waits for a PV except before reusing a P buffer
-// (PV(j-2)) and in the rare O rescale (PV(j-1)).
-//
+// Block g's scores go to S buffer g % 3; once the softmax has read them it writes
+// P(g) (bf16, two per column) over the buffer's first 64 columns, where the PV
+// MMA reads it.  S(g+3) overwrites the buffer only after PV(g) has completed,
+// and that wait is the S issuer's, not the softmax's: the softmax never waits
+// for a PV except in the rare O rescale (PV(g-1)).  With three buffers the S
+// MMAs run up to three blocks ahead, and the tensor core computes S(g+1),
+// S(g+2) and PV(g-1) while the softmax works on block g.
 // Softmax (base 2, c = scale*log2(e) folded into one FMA, MUFU ex2):
 //   each thread takes the max of its 64 scores; the two threads of a row are
 //   lanes i and i + 16 of one warp (TMEM 16x32bx2 accesses) and combine them with
 //   one shuffle;
 //   lazy rescale: the running max moves (and O, l are multiplied by
 //   2^(m_run - m_new)) only when the block max exceeds it by more than 8;
-//   p = 2^(s*c - m) -> bf16 -> TMEM P buffer; l accumulates the fp32 p.
+//   p = 2^(s*c - m) -> bf16 -> TMEM, over the S buffer; l accumulates the fp32 p.
 // Epilogue (the fused A2A): after the last PV each thread normalises its half of
 // the O row by 1/l and stores it with 16-byte st.global.v4 into the destination
 // row of the owning shard, then goes on to the next work unit.
@@ -82,18 +82,34 @@ __device__ int g_drain_failed = 0;
 //   2 clock64 when the piece's last P is written            3 clock64 when its last PV is done
 //   4 clock64 after the epilogue's stores are issued        5 (key blocks << 32) | piece kind
 // (clock64 is the SM's cycle counter: differences within one CTA are cycles).
+// After those words, for the first piece of each CTA and its first PHASE_BLOCKS
+// key blocks, PHASE_WORDS clock64 stamps per block (see phase_stamp's callers):
+// the softmax's steps (warp 0, lane 0) and the two MMA issuers' issue times.
 #ifdef XS_TILE_SPANS
 constexpr int SPAN_WORDS = 6;
+constexpr int PHASE_BLOCKS = 32;
+constexpr int PHASE_WORDS = 10;
 __device__ unsigned long long* g_spans = nullptr;
-__device__ int g_spans_per_cta = 0;
+__device__ int g_spans_ctas = 0;      // CTA slots of the buffer
+__device__ int g_spans_per_cta = 0;   // piece slots per CTA
 __device__ __forceinline__ void span_stamp(int k, int slot, unsigned long long v) {
     unsigned long long* s = g_spans;
-    if (s != nullptr && k < g_spans_per_cta && threadIdx.x == 0)
+    if (s != nullptr && k < g_spans_per_cta && static_cast<int>(blockIdx.x) < g_spans_ctas && threadIdx.x == 0)
         s[(static_cast<size_t>(blockIdx.x) * g_spans_per_cta + k) * SPAN_WORDS + slot] = v;
+}
+// A block-phase stamp of piece k, key block j, by the calling thread.
+__device__ __forceinline__ void phase_stamp(int k, int j, int slot) {
+    unsigned long long* s = g_spans;
+    if (s != nullptr && k == 0 && j < PHASE_BLOCKS && static_cast<int>(blockIdx.x) < g_spans_ctas) {
+        const size_t base = static_cast<size_t>(g_spans_ctas) * g_spans_per_cta * SPAN_WORDS;
+        s[base + (static_cast<size_t>(blockIdx.x) * PHASE_BLOCKS + j) * PHASE_WORDS + slot] =
+            static_cast<unsigned long long>(clock64());
+    }
 }
 __device__ __forceinline__ unsigned long long span_clock() { return static_cast<unsigned long long>(clock64()); }
 #else
 __device__ __forceinline__ void span_stamp(int, int, unsigned long long) {}
+__device__ __forceinline__ void phase_stamp(int, int, int) {}
 __device__ __forceinline__ unsigned long long span_clock() { return 0; }
 #endif
 
@@ -132,8 +148,8 @@ constexpr int WARP_TMA = 11;
 constexpr int WARP_MMA_S = 9;
 constexpr int WARP_MMA_PV = 10;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0;     // + 128 * buffer
-constexpr uint32_t P_COL = 256;   // + 64 * buffer
+constexpr uint32_t S_COL = 0;     // + 128 * buffer; P(g) over the first 64 columns of buffer g % 3
+constexpr int S_BUFS = 3;
 constexpr uint32_t O_COL = 384;
 constexpr int PANEL_BYTES = BLOCK_M * 128;  // 128 rows x 64 bf16
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
@@ -152,16 +168,15 @@ struct Cfg {
     // barrier indices
     static constexpr int B_Q_FULL = 0;                 // [2]  TMA -> MMA, per Q buffer
     static constexpr int B_Q_FREE = 2;                 // [2]  MMA -> TMA
-    static constexpr int B_S_FULL = 4;                 // [2]  MMA -> softmax, per S buffer
-    static constexpr int B_S_FREE = 6;                 // [2]  softmax -> MMA (scores read)
-    static constexpr int B_P_FULL = 8;                 // [2]  softmax -> MMA, per P buffer
-    static constexpr int B_P_FREE = 10;                // [2]  MMA -> softmax (PV done reading P)
-    static constexpr int B_O_FINAL = 12;               // [1]  MMA -> epilogue
-    static constexpr int B_O_FREE = 13;                // [1]  epilogue -> MMA
-    static constexpr int B_DRAIN = 14;                 // [1]  both issuers
-    static constexpr int B_KV_FULL = 15;               // [NS] TMA -> MMA
-    static constexpr int B_KV_FREE = 15 + KV_STAGES;   // [NS] MMA -> TMA
-    static constexpr int NUM_BARS = 15 + 2 * KV_STAGES;
+    static constexpr int B_S_FULL = 4;                 // [3]  S MMA -> softmax, per S buffer
+    static constexpr int B_P_FULL = 7;                 // [3]  softmax -> PV MMA (P written over the buffer)
+    static constexpr int B_P_FREE = 10;                // [3]  PV MMA -> S MMA / rescale (PV done: buffer free)
+    static constexpr int B_O_FINAL = 13;               // [1]  MMA -> epilogue
+    static constexpr int B_O_FREE = 14;                // [1]  epilogue -> MMA
+    static constexpr int B_DRAIN = 15;                 // [1]  both issuers
+    static constexpr int B_KV_FULL = 16;               // [NS] TMA -> MMA
+    static constexpr int B_KV_FREE = 16 + KV_STAGES;   // [NS] MMA -> TMA
+    static constexpr int NUM_BARS = 16 + 2 * KV_STAGES;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
@@ -509,7 +524,7 @@ __device__ __forceinline__ constexpr uint32_t k_step16(int kk) {
 // groups of 1024 B (SBO); 64-wide D panels are PANEL_BYTES apart (LBO).
 __device__ __forceinline__ constexpr uint32_t v_step16(int kk) { return static_cast<uint32_t>(kk * (2048 >> 4)); }
 
-// Issuer of S(j) = Q K_j^T (SS) into S buffer (block index) & 1.  One thread.
+// Issuer of S(j) = Q K_j^T (SS) into S buffer (block index) % 3.  One thread.
 template <int D, bool CAUSAL, bool VARLEN>
 __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* smem, uint32_t bar0,
                            uint32_t tmem_base, volatile int* abort_flag) {
@@ -520,6 +535,7 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
     const uint64_t qdesc0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);   // Q buffer 0
     const uint64_t kdesc0 = smem_desc_sw128(sbase + C::KV_OFF, 16, 1024);  // ring stage 0, as K
     uint32_t g = 0;      // key blocks over the CTA's lifetime
+    uint32_t sb = 0, sph = 0;   // S buffer of block g (g % 3) and its phase parity ((g / 3) & 1)
     uint32_t item0 = 0;  // first ring item of the current piece of work
     int u_iter = 0;
     bool ok = true;
@@ -534,10 +550,9 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
         if (ok && u_iter > 0) ok = thread_wait(bar(C::B_O_FINAL), (u_iter - 1) & 1, abort_flag, a.timeout_ns, u_iter);
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t gs = g + j;
-            const uint32_t sb = gs & 1;
-            // the softmax has read this S buffer's previous scores (block gs-2)
-            if (gs >= 2)
-                ok = thread_wait(bar(C::B_S_FREE + sb), ((gs >> 1) - 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
+            // the buffer's previous block (gs-3) is done: its P has been read by PV(gs-3)
+            if (gs >= S_BUFS)
+                ok = thread_wait(bar(C::B_P_FREE + sb), sph ^ 1u, abort_flag, a.timeout_ns, u_iter, j);
             const uint32_t item = item0 + ring_pos_k(j);
             const uint32_t stage = item % C::KV_STAGES;
             if (ok)
@@ -549,9 +564,14 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
             for (int kk = 0; kk < D / 16; ++kk)
                 mma_ss(tmem_base + S_COL + sb * 128u, desc_add(qdesc, k_step16(kk)), desc_add(kdesc, k_step16(kk)),
                        IDESC_QK, kk > 0);
+            phase_stamp(u_iter, j, 7);
             mma_commit(bar(C::B_S_FULL + sb));
             mma_commit(bar(C::B_KV_FREE + stage));
             if (j == n - 1) mma_commit(bar(C::B_Q_FREE + qb));
+            if (++sb == S_BUFS) {
+                sb = 0;
+                sph ^= 1u;
+            }
         }
         g += n;
         item0 += 2u * n;
@@ -562,7 +582,8 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
     drain_wait(bar(C::B_DRAIN), 0, a.timeout_ns > 20000000ull ? a.timeout_ns : 20000000ull);
 }
 
-// Issuer of PV(j): O += P(j) V_j (A = P buffer from TMEM).  One thread.
+// Issuer of PV(j): O += P(j) V_j (A = P(j), over the first 64 columns of S buffer
+// j % 3 in TMEM).  One thread.
 template <int D, bool CAUSAL, bool VARLEN>
 __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* smem, uint32_t bar0,
                             uint32_t tmem_base, volatile int* abort_flag) {
@@ -572,6 +593,7 @@ __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* s
     constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 1);
     const uint64_t vdesc0 = smem_desc_sw128(sbase + C::KV_OFF, PANEL_BYTES, 1024);  // ring stage 0, as V
     uint32_t g = 0;
+    uint32_t pb = 0, pph = 0;   // buffer of block g (g % 3) and its phase parity ((g / 3) & 1)
     uint32_t item0 = 0;
     int u_iter = 0;
     bool ok = true;
@@ -579,9 +601,7 @@ __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* s
     for (; ok && get_work<CAUSAL, VARLEN>(a, vt, u_iter, w); ++u_iter) {
         const int n = w.nb;
         for (int j = 0; j < n && ok; ++j) {
-            const uint32_t gj = g + j;
-            const uint32_t pb = gj & 1;
-            ok = thread_wait(bar(C::B_P_FULL + pb), (gj >> 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
+            ok = thread_wait(bar(C::B_P_FULL + pb), pph, abort_flag, a.timeout_ns, u_iter, j);
             // the epilogue has read the previous unit's O (PV(0) overwrites it)
             if (ok && j == 0 && u_iter > 0)
                 ok = thread_wait(bar(C::B_O_FREE), (u_iter - 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
@@ -594,11 +614,16 @@ __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* s
             const uint64_t vdesc = desc_add(vdesc0, stage * (C::TILE_BYTES >> 4));
 #pragma unroll
             for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-                mma_ts(tmem_base + O_COL, tmem_base + P_COL + pb * 64u + kk * 8, desc_add(vdesc, v_step16(kk)),
+                mma_ts(tmem_base + O_COL, tmem_base + S_COL + pb * 128u + kk * 8, desc_add(vdesc, v_step16(kk)),
                        IDESC_PV, (j > 0) || (kk > 0));
+            phase_stamp(u_iter, j, 8);
             mma_commit(bar(C::B_P_FREE + pb));
             mma_commit(bar(C::B_KV_FREE + stage));
             if (j == n - 1) mma_commit(bar(C::B_O_FINAL));
+            if (++pb == S_BUFS) {
+                pb = 0;
+                pph ^= 1u;
+            }
         }
         g += n;
         item0 += 2u * n;
@@ -794,6 +819,8 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
     const float c = a.c;
 
     uint32_t g = 0;
+    uint32_t sb = 0, sph = 0;    // S buffer of block g (g % 3) and its phase parity ((g / 3) & 1)
+    uint32_t pb = 2, pph = 1;    // the same for block g - 1 (the O rescale waits for PV(g-1))
     int u_iter = 0;
     bool ok = true;
     while (ok) {
@@ -812,9 +839,10 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
         }
         float m_run = 0.0f, l_run = 0.0f;
         for (int j = 0; j < n; ++j, ++g) {
-            const uint32_t sb = g & 1;
-            ok = warp_wait(bar(C::B_S_FULL + sb), (g >> 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
+            if (threadIdx.x == 0) phase_stamp(u_iter, j, 0);
+            ok = warp_wait(bar(C::B_S_FULL + sb), sph, abort_flag, a.timeout_ns, u_iter, j);
             if (!ok) break;
+            if (threadIdx.x == 0) phase_stamp(u_iter, j, 1);
             if (j == 0) {
                 span_stamp(u_iter, 0, globaltimer_ns());
                 span_stamp(u_iter, 1, span_clock());
@@ -824,8 +852,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             tmem_ld16x2_32<64>(t_base + S_COL + sb * 128u, sr[0]);
             tmem_ld16x2_32<64>(t_base + S_COL + sb * 128u + 32, sr[1]);
             tmem_wait_ld();
-            tc_fence_before();
-            warp_arrive(bar(C::B_S_FREE + sb));  // the MMA may now overwrite this S buffer
+            if (threadIdx.x == 0) phase_stamp(u_iter, j, 2);
             const int valid = valid0 - j * BLOCK_N;
             // Warp-uniform whenever the tail is (no causal mask).  On the causal
             // diagonal block the rows of a warp differ, and one vote keeps the
@@ -842,6 +869,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             // row max: the two halves of the row are lanes i and i ^ 16
             const float m_half = max64(sr);
             const float m_blk = fmaxf(m_half, __shfl_xor_sync(0xffffffffu, m_half, 16)) * c;
+            if (threadIdx.x == 0) phase_stamp(u_iter, j, 3);
             float m_use, alpha = 1.0f;
             bool rescale = false;
             if (j == 0) {
@@ -856,11 +884,12 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             uint32_t pk[32];
             const float sum = tail ? exp64<true>(sr, c, m_use, half * 64, valid, pk)
                                    : exp64<false>(sr, c, m_use, half * 64, valid, pk);
+            if (threadIdx.x == 0) phase_stamp(u_iter, j, 4);
             const bool redo = __any_sync(0xffffffffu, rescale);  // warp-uniform
             // Rescale of this thread's half of the O row (rare); PV(g-1) must have
             // completed first.  Warp-uniform: TMEM access is collective.
             if (redo) {
-                ok = warp_wait(bar(C::B_P_FREE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
+                ok = warp_wait(bar(C::B_P_FREE + pb), pph, abort_flag, a.timeout_ns, u_iter, j);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -873,19 +902,23 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                     tmem_st16x2_32<DH>(t_base + O_COL + q * 32, orr);
                 }
             }
-            // P buffer sb is free once PV(g-2) has completed.
-            if (g >= 2) {
-                ok = warp_wait(bar(C::B_P_FREE + sb), ((g >> 1) - 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
-                if (!ok) break;
-                tc_fence_after();
-            }
-            tmem_st16x2_32<32>(t_base + P_COL + sb * 64u, pk);
+            // P(g) over the first 64 columns of the scores just read (both halves
+            // of every row loaded: the loads above were warp-collective and waited)
+            if (threadIdx.x == 0) phase_stamp(u_iter, j, 5);
+            tmem_st16x2_32<32>(t_base + S_COL + sb * 128u, pk);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(C::B_P_FULL + sb));
+            if (threadIdx.x == 0) phase_stamp(u_iter, j, 6);
             if (j == n - 1) span_stamp(u_iter, 2, span_clock());
             l_run = l_run * alpha + sum;
             m_run = m_use;
+            pb = sb;
+            pph = sph;
+            if (++sb == S_BUFS) {
+                sb = 0;
+                sph ^= 1u;
+            }
         }
         if (!ok) break;
         // ---- epilogue: the owner of this tile stores it to the destination shard
@@ -973,8 +1006,9 @@ __device__ __forceinline__ void attn_body(const CUtensorMap* tq, const CUtensorM
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar0 + 8 * (C::B_Q_FULL + i), 1);   // (index 1 unused when Q_BUFS == 1)
             mbar_init(bar0 + 8 * (C::B_Q_FREE + i), 1);
+        }
+        for (int i = 0; i < S_BUFS; ++i) {
             mbar_init(bar0 + 8 * (C::B_S_FULL + i), 1);
-            mbar_init(bar0 + 8 * (C::B_S_FREE + i), NUM_SOFTMAX_WARPS);
             mbar_init(bar0 + 8 * (C::B_P_FULL + i), NUM_SOFTMAX_WARPS);
             mbar_init(bar0 + 8 * (C::B_P_FREE + i), 1);
         }
@@ -1162,8 +1196,9 @@ template cudaError_t launch_attn<128>(const CUtensorMap&, const CUtensorMap&, co
                                       int, bool, cudaStream_t);
 
 #ifdef XS_TILE_SPANS
-cudaError_t set_tile_spans(unsigned long long* buf, int per_cta) {
+cudaError_t set_tile_spans(unsigned long long* buf, int ctas, int per_cta) {
     cudaError_t e = cudaMemcpyToSymbol(g_spans, &buf, sizeof buf);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_spans_ctas, &ctas, sizeof ctas);
     if (e != cudaSuccess) return e;
     return cudaMemcpyToSymbol(g_spans_per_cta, &per_cta, sizeof per_cta);
 }

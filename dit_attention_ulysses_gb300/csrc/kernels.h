@@ -136,8 +136,8 @@ cudaError_t read_and_clear_device_error(int* value, DeviceErrorInfo* info, int* 
 
 #ifdef XS_TILE_SPANS
 // Instrumented build only: where the per-tile timestamps go (device buffer of
-// grid * per_cta * 6 words; NULL stops recording).
-cudaError_t set_tile_spans(unsigned long long* buf, int per_cta);
+// ctas * (per_cta * 6 + 32 * 10) words; NULL stops recording).
+cudaError_t set_tile_spans(unsigned long long* buf, int ctas, int per_cta);
 #endif
 
 struct RelayoutArgs {

@@ -18,6 +18,13 @@ microseconds: the block period (first scores to last P, per key block), the PV
 tail (last P to last PV done), the epilogue span (last PV done to stores
 issued: the fused All-to-All's cost on the critical path) and the refill (stores
 issued to the next piece's first scores in the same CTA).
+
+For the first piece of every CTA and its first PHASE_BLOCKS key blocks the build
+also records PHASE_WORDS clock64 stamps per block: the softmax's steps (warp 0,
+lane 0: 0 before the scores wait, 1 scores seen, 2 scores loaded from tensor
+memory, 3 row max combined, 4 exponentials done, 5 O rescaled if it had to be, 6 P stored and
+signalled) and the issue times of the block's S MMAs (7) and PV MMAs (8).
+``summarize_phases`` gives the median duration of each step.
 """
 from __future__ import annotations
 
@@ -26,6 +33,8 @@ import ctypes
 import numpy as np
 
 SPAN_WORDS = 6
+PHASE_BLOCKS = 32
+PHASE_WORDS = 10
 
 
 def parse(stamps: np.ndarray) -> list[dict]:
@@ -76,13 +85,35 @@ def summarize(stamps: np.ndarray, sm_ghz: float) -> dict:
             "first_to_last_start_us": (max(starts) - min(starts)) / 1e3 if starts else None}
 
 
+def summarize_phases(phases: np.ndarray, first_block: int = 2) -> dict:
+    """Block-phase stamps [grid, PHASE_BLOCKS, PHASE_WORDS] -> median cycles of each
+    softmax step over blocks >= first_block (past the pipeline fill) of every CTA."""
+    ph = np.asarray(phases, dtype=np.int64)
+    rows = []
+    for cta in range(ph.shape[0]):
+        for j in range(first_block, ph.shape[1] - 1):
+            a, b = ph[cta, j], ph[cta, j + 1]
+            if a[0] == 0 or a[6] == 0 or b[0] == 0:
+                continue
+            rows.append({"wait_scores": a[1] - a[0], "load_scores": a[2] - a[1], "row_max": a[3] - a[2],
+                         "exponentials": a[4] - a[3], "rescale_o": a[5] - a[4], "store_p": a[6] - a[5],
+                         "to_next_block": b[0] - a[6], "period": b[0] - a[0],
+                         "s_issued_to_seen": a[1] - a[7], "p_signalled_to_pv_issued": a[8] - a[6]})
+    if not rows:
+        return {"blocks": 0}
+    out = {"blocks": len(rows)}
+    for k in rows[0]:
+        out[k] = float(np.median([r[k] for r in rows]))
+    return out
+
+
 def load():
     """The instrumented library (built here if needed), with the entry points used."""
     from . import _build
     path = _build.build(variant="spans")
     lib = ctypes.CDLL(path)
     lib.xs_attn_set_tile_spans.restype = ctypes.c_int
-    lib.xs_attn_set_tile_spans.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.xs_attn_set_tile_spans.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
     lib.xs_attn_fwd_balanced.restype = ctypes.c_int
     lib.xs_attn_fwd_balanced.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p)] + \
         [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
@@ -93,12 +124,14 @@ def load():
 
 def record(q, k, v, outs, layout: int, scale: float, per_cta: int, workspace=None):
     """One launch of the instrumented kernel (xs_attn_fwd_balanced's arguments, torch
-    tensors on the current device); returns the stamps [grid, per_cta, 6] as uint64."""
+    tensors on the current device); returns the stamps [grid, per_cta, 6] and the
+    block-phase stamps [grid, PHASE_BLOCKS, PHASE_WORDS], both uint64."""
     import torch
     lib = load()
     sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-    buf = torch.zeros((sms, per_cta, SPAN_WORDS), dtype=torch.int64, device=q.device)
-    if lib.xs_attn_set_tile_spans(buf.data_ptr(), per_cta) != 0:
+    n_spans = sms * per_cta * SPAN_WORDS
+    buf = torch.zeros(n_spans + sms * PHASE_BLOCKS * PHASE_WORDS, dtype=torch.int64, device=q.device)
+    if lib.xs_attn_set_tile_spans(buf.data_ptr(), sms, per_cta) != 0:
         raise RuntimeError("xs_attn_set_tile_spans failed")
     B, S, H, D = q.shape
     ptrs = (ctypes.c_void_p * len(outs))(*[o.data_ptr() for o in outs])
@@ -108,5 +141,7 @@ def record(q, k, v, outs, layout: int, scale: float, per_cta: int, workspace=Non
                                   scale, wp, wn, stream)
     if rc != 0 or lib.xs_attn_get_device_error(stream) != 0:
         raise RuntimeError(f"instrumented launch failed ({rc})")
-    lib.xs_attn_set_tile_spans(None, 0)
-    return buf.cpu().numpy().view(np.uint64)
+    lib.xs_attn_set_tile_spans(None, 0, 0)
+    words = buf.cpu().numpy().view(np.uint64)
+    return (words[:n_spans].reshape(sms, per_cta, SPAN_WORDS),
+            words[n_spans:].reshape(sms, PHASE_BLOCKS, PHASE_WORDS))

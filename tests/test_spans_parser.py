@@ -38,3 +38,20 @@ def test_summary_recovers_the_constructed_spans():
     assert c["refill"]["n"] == 3 and c["refill"]["p50"] == 1500       # 2 in CTA 0, 1 in CTA 1
     assert abs(s["us"]["epilogue"]["p50"] - 1.0) < 1e-12                 # 2000 cycles at 2 GHz
     assert s["first_to_last_start_us"] == (17 * 2) / 1e3                 # ns -> us
+
+
+def test_block_phase_summary():
+    from dit_attention_ulysses_gb300.spans import PHASE_BLOCKS, PHASE_WORDS, summarize_phases
+    ph = np.zeros((3, PHASE_BLOCKS, PHASE_WORDS), dtype=np.uint64)
+    steps = [0, 100, 170, 260, 900, 940, 1000]          # cumulative cycles of stamps 0..6 in a block
+    for cta in range(3):
+        for j in range(PHASE_BLOCKS):
+            t0 = 5000 + 1500 * j
+            ph[cta, j, :7] = [t0 + d for d in steps]
+            ph[cta, j, 7] = t0 - 400                      # S MMAs issued 500 cycles before they are seen
+            ph[cta, j, 8] = t0 + 1000 + 60                # PV issued 60 cycles after P is signalled
+    s = summarize_phases(ph)
+    assert s["blocks"] == 3 * (PHASE_BLOCKS - 3)
+    assert (s["wait_scores"], s["load_scores"], s["row_max"], s["exponentials"]) == (100, 70, 90, 640)
+    assert (s["rescale_o"], s["store_p"], s["to_next_block"], s["period"]) == (40, 60, 500, 1500)
+    assert s["s_issued_to_seen"] == 500 and s["p_signalled_to_pv_issued"] == 60
