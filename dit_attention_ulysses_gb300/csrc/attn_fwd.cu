@@ -82,13 +82,16 @@ __device__ int g_drain_failed = 0;
 //   2 clock64 when the piece's last P is written            3 clock64 when its last PV is done
 //   4 clock64 after the epilogue's stores are issued        5 (key blocks << 32) | piece kind
 // (clock64 is the SM's cycle counter: differences within one CTA are cycles).
-// After those words, for the first piece of each CTA and its first PHASE_BLOCKS
-// key blocks, PHASE_WORDS clock64 stamps per block (see phase_stamp's callers):
-// the softmax's steps (warp 0, lane 0) and the two MMA issuers' issue times.
+// After those words, for the first piece of each CTA and its key blocks
+// PHASE_J0 .. PHASE_J0 + PHASE_BLOCKS - 1 (past the pipeline fill of the launch),
+// PHASE_WORDS clock64 stamps per block (see phase_stamp's callers): the
+// softmax's steps (warps 0 and 4, lane 0), the MMA issuers' waits and issue
+// times and the producer's load issue times.
 #ifdef XS_TILE_SPANS
 constexpr int SPAN_WORDS = 6;
+constexpr int PHASE_J0 = 8;
 constexpr int PHASE_BLOCKS = 32;
-constexpr int PHASE_WORDS = 10;
+constexpr int PHASE_WORDS = 16;
 __device__ unsigned long long* g_spans = nullptr;
 __device__ int g_spans_ctas = 0;      // CTA slots of the buffer
 __device__ int g_spans_per_cta = 0;   // piece slots per CTA
@@ -97,19 +100,24 @@ __device__ __forceinline__ void span_stamp(int k, int slot, unsigned long long v
     if (s != nullptr && k < g_spans_per_cta && static_cast<int>(blockIdx.x) < g_spans_ctas && threadIdx.x == 0)
         s[(static_cast<size_t>(blockIdx.x) * g_spans_per_cta + k) * SPAN_WORDS + slot] = v;
 }
-// A block-phase stamp of piece k, key block j, by the calling thread.
-__device__ __forceinline__ void phase_stamp(int k, int j, int slot) {
+// The block-phase rows of piece k for a thread that stamps (nullptr when it does
+// not): looked up once per piece, so that a stamp costs a clock read and a store.
+__device__ __forceinline__ unsigned long long* phase_rows(int k, bool stamps) {
     unsigned long long* s = g_spans;
-    if (s != nullptr && k == 0 && j < PHASE_BLOCKS && static_cast<int>(blockIdx.x) < g_spans_ctas) {
-        const size_t base = static_cast<size_t>(g_spans_ctas) * g_spans_per_cta * SPAN_WORDS;
-        s[base + (static_cast<size_t>(blockIdx.x) * PHASE_BLOCKS + j) * PHASE_WORDS + slot] =
-            static_cast<unsigned long long>(clock64());
-    }
+    if (s == nullptr || k != 0 || !stamps || static_cast<int>(blockIdx.x) >= g_spans_ctas) return nullptr;
+    return s + static_cast<size_t>(g_spans_ctas) * g_spans_per_cta * SPAN_WORDS +
+           static_cast<size_t>(blockIdx.x) * PHASE_BLOCKS * PHASE_WORDS;
+}
+// A block-phase stamp of key block j.
+__device__ __forceinline__ void phase_stamp(unsigned long long* rows, int j, int slot) {
+    if (rows != nullptr && static_cast<unsigned>(j - PHASE_J0) < static_cast<unsigned>(PHASE_BLOCKS))
+        rows[(j - PHASE_J0) * PHASE_WORDS + slot] = static_cast<unsigned long long>(clock64());
 }
 __device__ __forceinline__ unsigned long long span_clock() { return static_cast<unsigned long long>(clock64()); }
 #else
 __device__ __forceinline__ void span_stamp(int, int, unsigned long long) {}
-__device__ __forceinline__ void phase_stamp(int, int, int) {}
+__device__ __forceinline__ unsigned long long* phase_rows(int, bool) { return nullptr; }
+__device__ __forceinline__ void phase_stamp(unsigned long long*, int, int) {}
 __device__ __forceinline__ unsigned long long span_clock() { return 0; }
 #endif
 
@@ -460,6 +468,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
     Work w;
     for (; ok && get_work<CAUSAL, VARLEN>(a, vt, u_iter, w); ++u_iter) {
         const int b = w.b, h = w.h, qt = w.qt;
+        unsigned long long* const ph = phase_rows(u_iter, true);
         const int qb = u_iter % C::Q_BUFS;
         if (u_iter >= C::Q_BUFS)
             ok = thread_wait(bar(C::B_Q_FREE + qb), ((u_iter / C::Q_BUFS) - 1) & 1, abort_flag, a.timeout_ns, u_iter);
@@ -498,6 +507,7 @@ __device__ void producer_role(const CUtensorMap* tq, const CUtensorMap* tk, cons
                 tma_load_4d(sbase + C::KV_OFF + stage * C::TILE_BYTES + pnl * PANEL_BYTES, kv_map,
                             bar(C::B_KV_FULL + stage), pnl * 64, a.h0 + h, kv_row, b);
             ++item;
+            phase_stamp(ph, blk - w.k0, is_v ? 14 : 13);
         }
     }
     if (!ok) {
@@ -541,6 +551,7 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
     bool ok = true;
     Work w;
     for (; ok && get_work<CAUSAL, VARLEN>(a, vt, u_iter, w); ++u_iter) {
+        unsigned long long* const ph = phase_rows(u_iter, true);
         const int n = w.nb;
         const int qb = u_iter % C::Q_BUFS;
         const uint64_t qdesc = desc_add(qdesc0, qb * (C::TILE_BYTES >> 4));
@@ -553,10 +564,12 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
             // the buffer's previous block (gs-3) is done: its P has been read by PV(gs-3)
             if (gs >= S_BUFS)
                 ok = thread_wait(bar(C::B_P_FREE + sb), sph ^ 1u, abort_flag, a.timeout_ns, u_iter, j);
+            phase_stamp(ph, j, 11);
             const uint32_t item = item0 + ring_pos_k(j);
             const uint32_t stage = item % C::KV_STAGES;
             if (ok)
                 ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns, u_iter, j);
+            phase_stamp(ph, j, 12);
             if (!ok) break;
             tc_fence_after();
             const uint64_t kdesc = desc_add(kdesc0, stage * (C::TILE_BYTES >> 4));
@@ -564,7 +577,7 @@ __device__ void mma_s_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* sm
             for (int kk = 0; kk < D / 16; ++kk)
                 mma_ss(tmem_base + S_COL + sb * 128u, desc_add(qdesc, k_step16(kk)), desc_add(kdesc, k_step16(kk)),
                        IDESC_QK, kk > 0);
-            phase_stamp(u_iter, j, 7);
+            phase_stamp(ph, j, 7);
             mma_commit(bar(C::B_S_FULL + sb));
             mma_commit(bar(C::B_KV_FREE + stage));
             if (j == n - 1) mma_commit(bar(C::B_Q_FREE + qb));
@@ -599,9 +612,11 @@ __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* s
     bool ok = true;
     Work w;
     for (; ok && get_work<CAUSAL, VARLEN>(a, vt, u_iter, w); ++u_iter) {
+        unsigned long long* const ph = phase_rows(u_iter, true);
         const int n = w.nb;
         for (int j = 0; j < n && ok; ++j) {
             ok = thread_wait(bar(C::B_P_FULL + pb), pph, abort_flag, a.timeout_ns, u_iter, j);
+            phase_stamp(ph, j, 9);
             // the epilogue has read the previous unit's O (PV(0) overwrites it)
             if (ok && j == 0 && u_iter > 0)
                 ok = thread_wait(bar(C::B_O_FREE), (u_iter - 1) & 1, abort_flag, a.timeout_ns, u_iter, j);
@@ -609,6 +624,7 @@ __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* s
             const uint32_t stage = item % C::KV_STAGES;
             if (ok)
                 ok = thread_wait(bar(C::B_KV_FULL + stage), (item / C::KV_STAGES) & 1, abort_flag, a.timeout_ns, u_iter, j);
+            phase_stamp(ph, j, 10);
             if (!ok) break;
             tc_fence_after();
             const uint64_t vdesc = desc_add(vdesc0, stage * (C::TILE_BYTES >> 4));
@@ -616,7 +632,7 @@ __device__ void mma_pv_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* s
             for (int kk = 0; kk < BLOCK_N / 16; ++kk)
                 mma_ts(tmem_base + O_COL, tmem_base + S_COL + pb * 128u + kk * 8, desc_add(vdesc, v_step16(kk)),
                        IDESC_PV, (j > 0) || (kk > 0));
-            phase_stamp(u_iter, j, 8);
+            phase_stamp(ph, j, 8);
             mma_commit(bar(C::B_P_FREE + pb));
             mma_commit(bar(C::B_KV_FREE + stage));
             if (j == n - 1) mma_commit(bar(C::B_O_FINAL));
@@ -838,11 +854,13 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                 valid0 = seq_len - w.k0 * BLOCK_N;
         }
         float m_run = 0.0f, l_run = 0.0f;
+        unsigned long long* const ph = phase_rows(u_iter, threadIdx.x == 0);
+        unsigned long long* const ph4 = phase_rows(u_iter, threadIdx.x == 128);
         for (int j = 0; j < n; ++j, ++g) {
-            if (threadIdx.x == 0) phase_stamp(u_iter, j, 0);
+            phase_stamp(ph, j, 0);
             ok = warp_wait(bar(C::B_S_FULL + sb), sph, abort_flag, a.timeout_ns, u_iter, j);
             if (!ok) break;
-            if (threadIdx.x == 0) phase_stamp(u_iter, j, 1);
+            phase_stamp(ph, j, 1);
             if (j == 0) {
                 span_stamp(u_iter, 0, globaltimer_ns());
                 span_stamp(u_iter, 1, span_clock());
@@ -852,7 +870,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             tmem_ld16x2_32<64>(t_base + S_COL + sb * 128u, sr[0]);
             tmem_ld16x2_32<64>(t_base + S_COL + sb * 128u + 32, sr[1]);
             tmem_wait_ld();
-            if (threadIdx.x == 0) phase_stamp(u_iter, j, 2);
+            phase_stamp(ph, j, 2);
             const int valid = valid0 - j * BLOCK_N;
             // Warp-uniform whenever the tail is (no causal mask).  On the causal
             // diagonal block the rows of a warp differ, and one vote keeps the
@@ -869,7 +887,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             // row max: the two halves of the row are lanes i and i ^ 16
             const float m_half = max64(sr);
             const float m_blk = fmaxf(m_half, __shfl_xor_sync(0xffffffffu, m_half, 16)) * c;
-            if (threadIdx.x == 0) phase_stamp(u_iter, j, 3);
+            phase_stamp(ph, j, 3);
             float m_use, alpha = 1.0f;
             bool rescale = false;
             if (j == 0) {
@@ -884,7 +902,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             uint32_t pk[32];
             const float sum = tail ? exp64<true>(sr, c, m_use, half * 64, valid, pk)
                                    : exp64<false>(sr, c, m_use, half * 64, valid, pk);
-            if (threadIdx.x == 0) phase_stamp(u_iter, j, 4);
+            phase_stamp(ph, j, 4);
             const bool redo = __any_sync(0xffffffffu, rescale);  // warp-uniform
             // Rescale of this thread's half of the O row (rare); PV(g-1) must have
             // completed first.  Warp-uniform: TMEM access is collective.
@@ -904,12 +922,13 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             }
             // P(g) over the first 64 columns of the scores just read (both halves
             // of every row loaded: the loads above were warp-collective and waited)
-            if (threadIdx.x == 0) phase_stamp(u_iter, j, 5);
+            phase_stamp(ph, j, 5);
             tmem_st16x2_32<32>(t_base + S_COL + sb * 128u, pk);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(C::B_P_FULL + sb));
-            if (threadIdx.x == 0) phase_stamp(u_iter, j, 6);
+            phase_stamp(ph, j, 6);
+            phase_stamp(ph4, j, 15);
             if (j == n - 1) span_stamp(u_iter, 2, span_clock());
             l_run = l_run * alpha + sum;
             m_run = m_use;

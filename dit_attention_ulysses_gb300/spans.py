@@ -19,11 +19,16 @@ tail (last P to last PV done), the epilogue span (last PV done to stores
 issued: the fused All-to-All's cost on the critical path) and the refill (stores
 issued to the next piece's first scores in the same CTA).
 
-For the first piece of every CTA and its first PHASE_BLOCKS key blocks the build
-also records PHASE_WORDS clock64 stamps per block: the softmax's steps (warp 0,
+For the first piece of every CTA and its key blocks PHASE_J0 .. PHASE_J0 +
+PHASE_BLOCKS - 1 (past the launch's pipeline fill) the build also records
+PHASE_WORDS clock64 stamps per block: the softmax's steps (warp 0,
 lane 0: 0 before the scores wait, 1 scores seen, 2 scores loaded from tensor
 memory, 3 row max combined, 4 exponentials done, 5 O rescaled if it had to be, 6 P stored and
-signalled) and the issue times of the block's S MMAs (7) and PV MMAs (8).
+signalled), the S issuer (11 buffer free seen, 12 K tile seen, 7 S MMAs issued), the
+PV issuer (9 P seen, 10 V tile seen, 8 PV MMAs issued), the producer (13 K tile
+load issued, 14 V tile load issued) and warp 4, lane 0 (15 P stored and
+signalled: warp 4 shares warp 0's sub-partition and takes the other 16 rows of
+its lane quarter).
 ``summarize_phases`` gives the median duration of each step.
 """
 from __future__ import annotations
@@ -33,8 +38,9 @@ import ctypes
 import numpy as np
 
 SPAN_WORDS = 6
+PHASE_J0 = 8
 PHASE_BLOCKS = 32
-PHASE_WORDS = 10
+PHASE_WORDS = 16
 
 
 def parse(stamps: np.ndarray) -> list[dict]:
@@ -85,9 +91,9 @@ def summarize(stamps: np.ndarray, sm_ghz: float) -> dict:
             "first_to_last_start_us": (max(starts) - min(starts)) / 1e3 if starts else None}
 
 
-def summarize_phases(phases: np.ndarray, first_block: int = 2) -> dict:
+def summarize_phases(phases: np.ndarray, first_block: int = 0) -> dict:
     """Block-phase stamps [grid, PHASE_BLOCKS, PHASE_WORDS] -> median cycles of each
-    softmax step over blocks >= first_block (past the pipeline fill) of every CTA."""
+    softmax step over the recorded blocks >= first_block of every CTA."""
     ph = np.asarray(phases, dtype=np.int64)
     rows = []
     for cta in range(ph.shape[0]):
@@ -98,7 +104,12 @@ def summarize_phases(phases: np.ndarray, first_block: int = 2) -> dict:
             rows.append({"wait_scores": a[1] - a[0], "load_scores": a[2] - a[1], "row_max": a[3] - a[2],
                          "exponentials": a[4] - a[3], "rescale_o": a[5] - a[4], "store_p": a[6] - a[5],
                          "to_next_block": b[0] - a[6], "period": b[0] - a[0],
-                         "s_issued_to_seen": a[1] - a[7], "p_signalled_to_pv_issued": a[8] - a[6]})
+                         "s_issued_to_seen": a[1] - a[7], "p_signalled_to_pv_issued": a[8] - a[6],
+                         "warp4_minus_warp0_p_signalled": a[15] - a[6],
+                         "pv_sees_p_after_warp0": a[9] - a[6], "pv_sees_v_after_p": a[10] - a[9],
+                         "pv_issue_after_v": a[8] - a[10], "v_load_to_seen": a[10] - a[14],
+                         "s_buffer_free_after_softmax_start": a[11] - a[0], "s_sees_k_after_free": a[12] - a[11],
+                         "s_issue_after_k": a[7] - a[12], "k_load_to_seen": a[12] - a[13]})
     if not rows:
         return {"blocks": 0}
     out = {"blocks": len(rows)}
