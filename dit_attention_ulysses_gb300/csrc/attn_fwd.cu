@@ -85,13 +85,13 @@ __device__ int g_drain_failed = 0;
 // After those words, for the first piece of each CTA and its key blocks
 // PHASE_J0 .. PHASE_J0 + PHASE_BLOCKS - 1 (past the pipeline fill of the launch),
 // PHASE_WORDS clock64 stamps per block (see phase_stamp's callers): the
-// softmax's steps (warps 0 and 4, lane 0), the MMA issuers' waits and issue
-// times and the producer's load issue times.
+// softmax's steps (warp 0, lane 0), the time each softmax warp signals its P,
+// the MMA issuers' waits and issue times and the producer's load issue times.
 #ifdef XS_TILE_SPANS
 constexpr int SPAN_WORDS = 6;
 constexpr int PHASE_J0 = 8;
 constexpr int PHASE_BLOCKS = 32;
-constexpr int PHASE_WORDS = 16;
+constexpr int PHASE_WORDS = 24;
 __device__ unsigned long long* g_spans = nullptr;
 __device__ int g_spans_ctas = 0;      // CTA slots of the buffer
 __device__ int g_spans_per_cta = 0;   // piece slots per CTA
@@ -161,6 +161,7 @@ constexpr int S_BUFS = 3;
 constexpr uint32_t O_COL = 384;
 constexpr int PANEL_BYTES = BLOCK_M * 128;  // 128 rows x 64 bf16
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
+constexpr uint32_t WAIT_CHECK_EVERY = 16;   // probes between time-limit checks (a power of two)
 
 template <int D>
 struct Cfg {
@@ -191,26 +192,32 @@ struct Cfg {
 };
 
 // Bounded wait, executed by a whole warp; the result is warp-uniform.  The
-// first probe is a non-blocking test; after it the time limit is checked before
-// every further probe, and those probes are mbarrier.try_wait without a time
-// hint (the hardware's own short suspend limit: a waiting role resumes as soon
-// as the phase completes, which measured 1-5 % faster per launch than a 200 us
-// hint).  A limit of 0 therefore gives up at the first wait that is not already
-// over.  On expiry the wait records (barrier, parity, piece,
-// block) as the launch's first error, unless one is recorded already.
+// first probe is a non-blocking test; the further probes are mbarrier.try_wait
+// without a time hint (the hardware's own short suspend limit: a waiting role
+// resumes as soon as the phase completes, which measured 1-5 % faster per launch
+// than a 200 us hint).  The abort flag and the time limit are looked at before
+// the first try_wait's retry and then every WAIT_CHECK_EVERY probes: a
+// %globaltimer read costs more than a probe, and a read between the phase's
+// completion and the next probe delays the waiter by that much.  A limit of 0
+// therefore gives up after WAIT_CHECK_EVERY probes of the first wait that is not
+// already over.  On expiry the wait records (barrier, parity, piece, block) as
+// the launch's first error, unless one is recorded already.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t timeout_ns, int unit = -1, int blk = -1) {
     bool ok = mbar_test_wait(bar, parity);
     if (!__all_sync(0xffffffffu, ok)) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!ok) {
+        uint64_t t0 = 0;
+        for (uint32_t n = 0; !ok; ++n) {
+            ok = mbar_try_wait(bar, parity);
+            if (ok || (n & (WAIT_CHECK_EVERY - 1)) != 0) continue;
             if (*abort_flag) break;
-            if (expired(t0, timeout_ns)) {
+            if (n == 0) {
+                t0 = globaltimer_ns();
+            } else if (expired(t0, timeout_ns)) {
                 *abort_flag = 1;
                 report_error(XS_DEVICE_TIMEOUT_CODE, static_cast<int>(bar), static_cast<int>(parity), unit, blk);
                 break;
             }
-            ok = mbar_try_wait(bar, parity);
         }
         ok = __all_sync(0xffffffffu, ok);
     }
@@ -222,15 +229,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                             uint64_t timeout_ns, int unit = -1, int blk = -1) {
     if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    uint64_t t0 = 0;
+    for (uint32_t n = 0;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & (WAIT_CHECK_EVERY - 1)) != 0) continue;
         if (*abort_flag) return false;
-        if (expired(t0, timeout_ns)) {
+        if (n == 0) {
+            t0 = globaltimer_ns();
+        } else if (expired(t0, timeout_ns)) {
             *abort_flag = 1;
             report_error(XS_DEVICE_TIMEOUT_CODE, static_cast<int>(bar), static_cast<int>(parity), unit, blk);
             return false;
         }
-        if (mbar_try_wait(bar, parity)) return true;
     }
 }
 
@@ -855,7 +865,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
         }
         float m_run = 0.0f, l_run = 0.0f;
         unsigned long long* const ph = phase_rows(u_iter, threadIdx.x == 0);
-        unsigned long long* const ph4 = phase_rows(u_iter, threadIdx.x == 128);
+        unsigned long long* const phw = phase_rows(u_iter, lane == 0);   // every softmax warp's lane 0
         for (int j = 0; j < n; ++j, ++g) {
             phase_stamp(ph, j, 0);
             ok = warp_wait(bar(C::B_S_FULL + sb), sph, abort_flag, a.timeout_ns, u_iter, j);
@@ -928,7 +938,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             tc_fence_before();
             warp_arrive(bar(C::B_P_FULL + sb));
             phase_stamp(ph, j, 6);
-            phase_stamp(ph4, j, 15);
+            phase_stamp(phw, j, 16 + warp);
             if (j == n - 1) span_stamp(u_iter, 2, span_clock());
             l_run = l_run * alpha + sum;
             m_run = m_use;

@@ -26,9 +26,9 @@ lane 0: 0 before the scores wait, 1 scores seen, 2 scores loaded from tensor
 memory, 3 row max combined, 4 exponentials done, 5 O rescaled if it had to be, 6 P stored and
 signalled), the S issuer (11 buffer free seen, 12 K tile seen, 7 S MMAs issued), the
 PV issuer (9 P seen, 10 V tile seen, 8 PV MMAs issued), the producer (13 K tile
-load issued, 14 V tile load issued) and warp 4, lane 0 (15 P stored and
-signalled: warp 4 shares warp 0's sub-partition and takes the other 16 rows of
-its lane quarter).
+load issued, 14 V tile load issued) and lane 0 of every softmax warp w (16 + w: P
+stored and signalled; warp w runs on sub-partition w % 4, beside warp w + 4 and
+one of the single-thread roles or the idle warp).
 ``summarize_phases`` gives the median duration of each step.
 """
 from __future__ import annotations
@@ -40,7 +40,7 @@ import numpy as np
 SPAN_WORDS = 6
 PHASE_J0 = 8
 PHASE_BLOCKS = 32
-PHASE_WORDS = 16
+PHASE_WORDS = 24
 
 
 def parse(stamps: np.ndarray) -> list[dict]:
@@ -105,7 +105,7 @@ def summarize_phases(phases: np.ndarray, first_block: int = 0) -> dict:
                          "exponentials": a[4] - a[3], "rescale_o": a[5] - a[4], "store_p": a[6] - a[5],
                          "to_next_block": b[0] - a[6], "period": b[0] - a[0],
                          "s_issued_to_seen": a[1] - a[7], "p_signalled_to_pv_issued": a[8] - a[6],
-                         "warp4_minus_warp0_p_signalled": a[15] - a[6],
+                         **{f"warp{w}_p_signalled_after_warp0": a[16 + w] - a[16] for w in range(1, 8)},
                          "pv_sees_p_after_warp0": a[9] - a[6], "pv_sees_v_after_p": a[10] - a[9],
                          "pv_issue_after_v": a[8] - a[10], "v_load_to_seen": a[10] - a[14],
                          "s_buffer_free_after_softmax_start": a[11] - a[0], "s_sees_k_after_free": a[12] - a[11],

@@ -53,11 +53,12 @@ def test_block_phase_summary():
             ph[cta, j, 9] = t0 + 1000 + 20                # the PV issuer sees P 20 cycles after warp 0's signal
             ph[cta, j, 10] = t0 + 1000 + 30               # ... and V 10 cycles later
             ph[cta, j, 14] = t0 - 2000                    # V load issued
-            ph[cta, j, 15] = t0 + 1000 + 5                # warp 4 signals 5 cycles after warp 0
+            ph[cta, j, 16] = t0 + 1000                    # warp 0 signals with stamp 6
+            ph[cta, j, 16 + 4] = t0 + 1000 + 5            # warp 4 signals 5 cycles after warp 0
     s = summarize_phases(ph)
     assert s["blocks"] == 3 * (PHASE_BLOCKS - 1)          # every recorded block but the last (no next block)
     assert (s["wait_scores"], s["load_scores"], s["row_max"], s["exponentials"]) == (100, 70, 90, 640)
     assert (s["rescale_o"], s["store_p"], s["to_next_block"], s["period"]) == (40, 60, 500, 1500)
     assert s["s_issued_to_seen"] == 500 and s["p_signalled_to_pv_issued"] == 60
     assert (s["pv_sees_p_after_warp0"], s["pv_sees_v_after_p"], s["pv_issue_after_v"]) == (20, 10, 30)
-    assert s["v_load_to_seen"] == 3030 and s["warp4_minus_warp0_p_signalled"] == 5
+    assert s["v_load_to_seen"] == 3030 and s["warp4_p_signalled_after_warp0"] == 5
