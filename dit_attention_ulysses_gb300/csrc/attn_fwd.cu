@@ -168,7 +168,7 @@ struct Cfg {
     static constexpr int TILE_BYTES = BLOCK_M * D * 2;
     static constexpr int PANELS = D / 64;
     static constexpr int Q_BUFS = (D == 128) ? 1 : 2;
-    static constexpr int KV_STAGES = (D == 128) ? 5 : 10;
+    static constexpr int KV_STAGES = (D == 128) ? 4 : 10;
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = Q_BUFS * TILE_BYTES;
     static constexpr int STAGE_OFF = KV_OFF + KV_STAGES * TILE_BYTES;  // epilogue staging, 2 KB per softmax warp
