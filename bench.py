@@ -587,14 +587,15 @@ def run_tile_spans(args):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     per_cta = -(-w.B * w.H * ((w.S + 127) // 128) // sms) + 2
     for _ in range(3):   # warm-up of the instrumented library, then the recorded launch
-        st, ph = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
+        st, ph, ep = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
     sampler = ClockSampler(0)
     sampler.start()
     t0 = time.time()
-    st, ph = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
+    st, ph, ep = spans.record(q, k, v, outs, xs.XS_LAYOUT_A2A, w.scale, per_cta, ws)
     clocks = sampler.stop(t0, time.time())
     ghz = (clocks.get("sm_mhz") or 2070.0) / 1e3
     print(json.dumps({"tile_spans": spans.summarize(st, ghz), "block_phases_cycles": spans.summarize_phases(ph),
+                      "epilogue_steps_cycles": spans.summarize_epilogue(ep),
                       "workload": w.name, "sm_ghz_assumed": ghz, "clocks": clocks,
                       "kernel_source": kernel_source_hash()}), flush=True)
 

@@ -87,11 +87,14 @@ __device__ int g_drain_failed = 0;
 // PHASE_WORDS clock64 stamps per block (see phase_stamp's callers): the
 // softmax's steps (warp 0, lane 0), the time each softmax warp signals its P,
 // the MMA issuers' waits and issue times and the producer's load issue times.
+// Last, EPI_WORDS clock64 stamps per CTA of warp 0's epilogue of its first
+// piece (see epi_stamp's callers).
 #ifdef XS_TILE_SPANS
 constexpr int SPAN_WORDS = 6;
 constexpr int PHASE_J0 = 8;
 constexpr int PHASE_BLOCKS = 32;
 constexpr int PHASE_WORDS = 24;
+constexpr int EPI_WORDS = 8;
 __device__ unsigned long long* g_spans = nullptr;
 __device__ int g_spans_ctas = 0;      // CTA slots of the buffer
 __device__ int g_spans_per_cta = 0;   // piece slots per CTA
@@ -113,11 +116,23 @@ __device__ __forceinline__ void phase_stamp(unsigned long long* rows, int j, int
     if (rows != nullptr && static_cast<unsigned>(j - PHASE_J0) < static_cast<unsigned>(PHASE_BLOCKS))
         rows[(j - PHASE_J0) * PHASE_WORDS + slot] = static_cast<unsigned long long>(clock64());
 }
+// The epilogue stamps of piece k for a thread that stamps (nullptr when it does not).
+__device__ __forceinline__ unsigned long long* epi_rows(int k, bool stamps) {
+    unsigned long long* s = g_spans;
+    if (s == nullptr || k != 0 || !stamps || static_cast<int>(blockIdx.x) >= g_spans_ctas) return nullptr;
+    return s + static_cast<size_t>(g_spans_ctas) * (g_spans_per_cta * SPAN_WORDS + PHASE_BLOCKS * PHASE_WORDS) +
+           static_cast<size_t>(blockIdx.x) * EPI_WORDS;
+}
+__device__ __forceinline__ void epi_stamp(unsigned long long* rows, int slot) {
+    if (rows != nullptr) rows[slot] = static_cast<unsigned long long>(clock64());
+}
 __device__ __forceinline__ unsigned long long span_clock() { return static_cast<unsigned long long>(clock64()); }
 #else
 __device__ __forceinline__ void span_stamp(int, int, unsigned long long) {}
 __device__ __forceinline__ unsigned long long* phase_rows(int, bool) { return nullptr; }
 __device__ __forceinline__ void phase_stamp(unsigned long long*, int, int) {}
+__device__ __forceinline__ unsigned long long* epi_rows(int, bool) { return nullptr; }
+__device__ __forceinline__ void epi_stamp(unsigned long long*, int) {}
 __device__ __forceinline__ unsigned long long span_clock() { return 0; }
 #endif
 
@@ -958,6 +973,8 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
         ok = warp_wait(bar(C::B_O_FINAL), u_iter & 1, abort_flag, a.timeout_ns, u_iter);
         if (!ok) break;
         span_stamp(u_iter, 3, span_clock());
+        unsigned long long* const pe = epi_rows(u_iter, threadIdx.x == 0);
+        epi_stamp(pe, 0);
         tc_fence_after();
         if (w.kind == WORK_FULL) {
             // Each lane holds half a row; stores straight from the lanes would
@@ -978,6 +995,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                 else
                     report_error(XS_DEVICE_BOUNDS_CODE, 2, p, s_row, h);
             }
+            epi_stamp(pe, 1);
             uint4* stage = reinterpret_cast<uint4*>(smem + C::STAGE_OFF + warp * 2048);
             const float inv_l = 1.0f / l_row;
 #pragma unroll
@@ -985,6 +1003,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                 uint32_t orr[32];
                 tmem_ld16x2_32<DH>(t_base + O_COL + q * 32, orr);
                 tmem_wait_ld();
+                epi_stamp(pe, 2 + 3 * q);
                 uint32_t wv[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -994,6 +1013,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                     stage[lane * 4 + (c4 ^ (lane & 3))] =
                         make_uint4(wv[4 * c4], wv[4 * c4 + 1], wv[4 * c4 + 2], wv[4 * c4 + 3]);
                 __syncwarp();
+                epi_stamp(pe, 3 + 3 * q);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int r = k * 8 + (lane >> 2);   // lane whose half row this lane stores a chunk of
@@ -1004,6 +1024,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
                         st_global_v4(reinterpret_cast<__nv_bfloat16*>(rp) + q * 32 + c4 * 8, v.x, v.y, v.z, v.w);
                 }
                 __syncwarp();   // the stage is rewritten by the next chunk
+                epi_stamp(pe, 4 + 3 * q);
             }
         } else {
             ok = split_epilogue<D>(a, w, t_base + O_COL, row, half, warp, m_run, l_row,

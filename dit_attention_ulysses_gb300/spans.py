@@ -30,6 +30,12 @@ load issued, 14 V tile load issued) and lane 0 of every softmax warp w (16 + w: 
 stored and signalled; warp w runs on sub-partition w % 4, beside warp w + 4 and
 one of the single-thread roles or the idle warp).
 ``summarize_phases`` gives the median duration of each step.
+
+Last, EPI_WORDS stamps per CTA of warp 0's epilogue of its first piece (when it
+is a whole tile): 0 last PV seen done, 1 destination row computed, then for each
+32-column chunk of the thread's half row (two at D = 128) its O loaded from
+tensor memory, its bf16 values staged in shared memory and its global stores
+issued.  ``summarize_epilogue`` gives the median of each step.
 """
 from __future__ import annotations
 
@@ -41,6 +47,7 @@ SPAN_WORDS = 6
 PHASE_J0 = 8
 PHASE_BLOCKS = 32
 PHASE_WORDS = 24
+EPI_WORDS = 8
 
 
 def parse(stamps: np.ndarray) -> list[dict]:
@@ -118,6 +125,24 @@ def summarize_phases(phases: np.ndarray, first_block: int = 0) -> dict:
     return out
 
 
+def summarize_epilogue(epi: np.ndarray) -> dict:
+    """Epilogue stamps [grid, EPI_WORDS] -> median cycles of each step over the CTAs
+    whose first piece ended in a whole-tile epilogue."""
+    e = np.asarray(epi, dtype=np.int64)
+    names = ["destination_row", "load_o_0", "stage_0", "stores_0", "load_o_1", "stage_1", "stores_1"]
+    rows = [r for r in e if r[0] != 0 and r[4] != 0]
+    if not rows:
+        return {"ctas": 0}
+    out = {"ctas": len(rows)}
+    for i, k in enumerate(names):
+        d = [r[i + 1] - r[i] for r in rows if r[i + 1] != 0]
+        if d:
+            out[k] = float(np.median(d))
+    last = [r[max(i for i in range(EPI_WORDS) if r[i] != 0)] - r[0] for r in rows]
+    out["total"] = float(np.median(last))
+    return out
+
+
 def load():
     """The instrumented library (built here if needed), with the entry points used."""
     from . import _build
@@ -135,13 +160,15 @@ def load():
 
 def record(q, k, v, outs, layout: int, scale: float, per_cta: int, workspace=None):
     """One launch of the instrumented kernel (xs_attn_fwd_balanced's arguments, torch
-    tensors on the current device); returns the stamps [grid, per_cta, 6] and the
-    block-phase stamps [grid, PHASE_BLOCKS, PHASE_WORDS], both uint64."""
+    tensors on the current device); returns the stamps [grid, per_cta, 6], the
+    block-phase stamps [grid, PHASE_BLOCKS, PHASE_WORDS] and the epilogue stamps
+    [grid, EPI_WORDS], all uint64."""
     import torch
     lib = load()
     sms = torch.cuda.get_device_properties(q.device).multi_processor_count
     n_spans = sms * per_cta * SPAN_WORDS
-    buf = torch.zeros(n_spans + sms * PHASE_BLOCKS * PHASE_WORDS, dtype=torch.int64, device=q.device)
+    n_phase = sms * PHASE_BLOCKS * PHASE_WORDS
+    buf = torch.zeros(n_spans + n_phase + sms * EPI_WORDS, dtype=torch.int64, device=q.device)
     if lib.xs_attn_set_tile_spans(buf.data_ptr(), sms, per_cta) != 0:
         raise RuntimeError("xs_attn_set_tile_spans failed")
     B, S, H, D = q.shape
@@ -155,4 +182,5 @@ def record(q, k, v, outs, layout: int, scale: float, per_cta: int, workspace=Non
     lib.xs_attn_set_tile_spans(None, 0, 0)
     words = buf.cpu().numpy().view(np.uint64)
     return (words[:n_spans].reshape(sms, per_cta, SPAN_WORDS),
-            words[n_spans:].reshape(sms, PHASE_BLOCKS, PHASE_WORDS))
+            words[n_spans:n_spans + n_phase].reshape(sms, PHASE_BLOCKS, PHASE_WORDS),
+            words[n_spans + n_phase:].reshape(sms, EPI_WORDS))

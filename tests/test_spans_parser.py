@@ -62,3 +62,15 @@ def test_block_phase_summary():
     assert s["s_issued_to_seen"] == 500 and s["p_signalled_to_pv_issued"] == 60
     assert (s["pv_sees_p_after_warp0"], s["pv_sees_v_after_p"], s["pv_issue_after_v"]) == (20, 10, 30)
     assert s["v_load_to_seen"] == 3030 and s["warp4_p_signalled_after_warp0"] == 5
+
+
+def test_epilogue_summary():
+    from dit_attention_ulysses_gb300.spans import EPI_WORDS, summarize_epilogue
+    ep = np.zeros((4, EPI_WORDS), dtype=np.uint64)
+    steps = [0, 300, 330, 400, 900, 930, 1000, 1500]     # cumulative cycles of stamps 0..7
+    for cta in range(3):
+        ep[cta] = [10000 * (cta + 1) + d for d in steps]
+    s = summarize_epilogue(ep)                              # CTA 3 recorded nothing
+    assert s["ctas"] == 3 and s["total"] == 1500
+    assert (s["destination_row"], s["load_o_0"], s["stage_0"], s["stores_0"]) == (300, 30, 70, 500)
+    assert (s["load_o_1"], s["stage_1"], s["stores_1"]) == (30, 70, 500)
