@@ -214,8 +214,7 @@ struct Cfg {
 // the first try_wait's retry and then every WAIT_CHECK_EVERY probes: a
 // %globaltimer read costs more than a probe, and a read between the phase's
 // completion and the next probe delays the waiter by that much.  A limit of 0
-// therefore gives up after WAIT_CHECK_EVERY probes of the first wait that is not
-// already over.  On expiry the wait records (barrier, parity, piece, block) as
+// gives up after the first try_wait of the first wait that is not already over.  On expiry the wait records (barrier, parity, piece, block) as
 // the launch's first error, unless one is recorded already.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t timeout_ns, int unit = -1, int blk = -1) {
@@ -226,9 +225,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
             ok = mbar_try_wait(bar, parity);
             if (ok || (n & (WAIT_CHECK_EVERY - 1)) != 0) continue;
             if (*abort_flag) break;
-            if (n == 0) {
-                t0 = globaltimer_ns();
-            } else if (expired(t0, timeout_ns)) {
+            if (n == 0) t0 = globaltimer_ns();
+            if (expired(t0, timeout_ns)) {
                 *abort_flag = 1;
                 report_error(XS_DEVICE_TIMEOUT_CODE, static_cast<int>(bar), static_cast<int>(parity), unit, blk);
                 break;
@@ -249,9 +247,8 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volat
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & (WAIT_CHECK_EVERY - 1)) != 0) continue;
         if (*abort_flag) return false;
-        if (n == 0) {
-            t0 = globaltimer_ns();
-        } else if (expired(t0, timeout_ns)) {
+        if (n == 0) t0 = globaltimer_ns();
+        if (expired(t0, timeout_ns)) {
             *abort_flag = 1;
             report_error(XS_DEVICE_TIMEOUT_CODE, static_cast<int>(bar), static_cast<int>(parity), unit, blk);
             return false;
