@@ -356,8 +356,9 @@ def xs_attn_varlen_fwd(q, k, v, seqlens, layout: int, outs, scale: float, causal
                        stream=None) -> None:
     """Attention over packed variable-length sequences: ``q``, ``k``, ``v`` are
     [T, H, D] bf16 holding sequences of lengths ``seqlens`` (host integers) back to
-    back; each row attends to its own sequence.  ``causal=True`` is refused
-    (XsError with XS_ERR_UNAVAILABLE): that form is disabled in this build.
+    back; each row attends to its own sequence (``causal=True``: to its own
+    sequence's keys up to its own position; run as one causal launch per
+    sequence).
     ``layout`` XS_LAYOUT_A2A (P shards [T/P, H, D]), XS_LAYOUT_CONTIGUOUS (one
     [T, H, D] tensor) or XS_LAYOUT_HEADS (P head shards [T, H/P, D])."""
     T, H, D = _thd(q, "q").shape

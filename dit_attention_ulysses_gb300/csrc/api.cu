@@ -625,9 +625,6 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
     }
     if (total != T || tiles > xs::MAX_VARLEN_TILES) return XS_ERR_SHAPE;
     if (tiles * static_cast<int64_t>(H) > INT32_MAX) return XS_ERR_SHAPE;   // units must fit an int
-    // The causal form is not launched: at 75,776 packed tokens its kernel ended
-    // in an unspecified launch failure whose cause is not established.
-    if (causal) return XS_ERR_UNAVAILABLE;
     xs::EpiParams epi;
     int n_out = 0;
     int64_t out_bytes = 0;
@@ -637,13 +634,37 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
     rc = validate_attn(q, k, v, outs, n_out, 1, T, H, D, layout == XS_LAYOUT_CONTIGUOUS ? 1 : P, scale, out_bytes,
                        need_div);
     if (rc != XS_OK) return rc;
+    if (causal) {
+        // The packed kernel's causal form is not launched (at 75,776 packed tokens
+        // it ended in an unspecified launch failure whose cause is not
+        // established).  The causal packed call runs as one causal launch per
+        // sequence instead: the sequence's rows of Q, K and V as [1, len, H, D]
+        // tensors, its output row s stored at packed row start + s of the layout.
+        const size_t row_bytes = static_cast<size_t>(H) * D * 2;
+        const cudaStream_t st = static_cast<cudaStream_t>(stream);
+        int start = 0;
+        for (int i = 0; i < n_seqs; ++i) {
+            const int L = seqlens[i];
+            if (L > 0) {
+                xs::EpiParams es = epi;
+                es.row0 = start;
+                const size_t off = static_cast<size_t>(start) * row_bytes;
+                rc = run_attention(static_cast<const char*>(q) + off, static_cast<const char*>(k) + off,
+                                   static_cast<const char*>(v) + off, nullptr, 0, es, 1, L, H, D, scale, nullptr, 0,
+                                   st, true);
+                if (rc != XS_OK) return rc;
+            }
+            start += L;
+        }
+        return XS_OK;
+    }
     DeviceInfo dev;
     if ((rc = device_info(&dev)) != XS_OK) return rc;
 
-    // The tile list, longest first: tile (i, t) reads ceil(len_i / 128) key blocks,
-    // or t + 1 when causal; ties keep sequence order, then query-tile order (the
-    // sort is stable), so without the mask a sequence's tiles stay together, tile 0
-    // first, which the kernel's head-major order within a sequence relies on.
+    // The tile list, longest first: tile (i, t) reads ceil(len_i / 128) key blocks;
+    // ties keep sequence order, then query-tile order (the sort is stable), so a
+    // sequence's tiles stay together, tile 0 first, which the kernel's head-major
+    // order within a sequence relies on.
     static thread_local xs::VarlenTable vt;   // 20 KB: kept off the stack
     vt.n_seqs = n_seqs;
     vt.cu[0] = 0;
@@ -652,10 +673,7 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
     for (int i = 0; i < n_seqs; ++i)
         for (int t = 0; t * 128 < seqlens[i]; ++t) vt.tile[n++] = (static_cast<unsigned>(i) << 16) | static_cast<unsigned>(t);
     vt.n_tiles = n;
-    auto blocks = [&](unsigned e) {
-        const int i = static_cast<int>(e >> 16), t = static_cast<int>(e & 0xffffu);
-        return causal ? t + 1 : (seqlens[i] + 127) / 128;
-    };
+    auto blocks = [&](unsigned e) { return (seqlens[e >> 16] + 127) / 128; };
     std::stable_sort(vt.tile, vt.tile + n, [&](unsigned x, unsigned y) { return blocks(x) > blocks(y); });
 
     xs::AttnArgs a;
@@ -676,8 +694,8 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
     if ((rc = encode_bshd(&tk, k, 1, T, H, D)) != XS_OK) return rc;
     if ((rc = encode_bshd(&tv, v, 1, T, H, D)) != XS_OK) return rc;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = (D == 128) ? xs::launch_attn_varlen<128>(tq, tk, tv, a, vt, causal != 0, grid, st)
-                                     : xs::launch_attn_varlen<64>(tq, tk, tv, a, vt, causal != 0, grid, st);
+    const cudaError_t e = (D == 128) ? xs::launch_attn_varlen<128>(tq, tk, tv, a, vt, grid, st)
+                                     : xs::launch_attn_varlen<64>(tq, tk, tv, a, vt, grid, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return XS_OK;
 }

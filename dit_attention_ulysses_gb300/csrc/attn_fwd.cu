@@ -794,8 +794,9 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
         l_all += ml.y * ex2_approx(ml.x - m_all);
     }
     const float inv_l = 1.0f / l_all;
-    const int s_row = w.qt * BLOCK_M + row;
-    bool store = s_row < a.S;
+    const int s_loc = w.qt * BLOCK_M + row;
+    const int s_row = a.epi.row0 + s_loc;
+    bool store = s_loc < a.S;
     __nv_bfloat16* dst = nullptr;
     if (store) {
         const int hg = a.h0_out + w.h;   // head in the output layout
@@ -981,7 +982,7 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             const int s_loc = qt * BLOCK_M + row;   // row within the sequence
             unsigned long long dst_row = 0;   // this lane's half row in the destination (0: past the sequence)
             if (s_loc < (VARLEN ? w.len : a.S)) {
-                const int s_row = (VARLEN ? w.row0 : 0) + s_loc;
+                const int s_row = (VARLEN ? w.row0 : a.epi.row0) + s_loc;
                 const int p = s_row / a.epi.Sl + h / a.epi.Hl;
                 const int s_dst = s_row % a.epi.Sl;
                 const int h_dst = h % a.epi.Hl;
@@ -1216,9 +1217,8 @@ cudaError_t launch_attn_causal(const CUtensorMap& tq, const CUtensorMap& tk, con
 
 template <int D>
 cudaError_t launch_attn_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const AttnArgs& args, const VarlenTable& vt, bool causal, int grid,
-                               cudaStream_t stream) {
-    auto kern = causal ? attn_varlen_kernel<D, true> : attn_varlen_kernel<D, false>;
+                               const AttnArgs& args, const VarlenTable& vt, int grid, cudaStream_t stream) {
+    auto kern = attn_varlen_kernel<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, args, vt);
@@ -1226,9 +1226,9 @@ cudaError_t launch_attn_varlen(const CUtensorMap& tq, const CUtensorMap& tk, con
 }
 
 template cudaError_t launch_attn_varlen<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                            const AttnArgs&, const VarlenTable&, bool, int, cudaStream_t);
+                                            const AttnArgs&, const VarlenTable&, int, cudaStream_t);
 template cudaError_t launch_attn_varlen<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                             const AttnArgs&, const VarlenTable&, bool, int, cudaStream_t);
+                                             const AttnArgs&, const VarlenTable&, int, cudaStream_t);
 template cudaError_t launch_attn_causal<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                             const AttnArgs&, int, cudaStream_t);
 template cudaError_t launch_attn_causal<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,

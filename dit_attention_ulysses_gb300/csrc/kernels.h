@@ -33,6 +33,7 @@ struct EpiParams {
     void* ptr[MAX_PTRS];
     int Sl;
     int Hl;
+    int row0;   // output row of the launch's row 0 (one sequence of a packed batch; else 0)
 };
 
 // Balanced ("stream-K") schedule of the tiles left over after the whole waves.
@@ -117,12 +118,13 @@ template <int D>
 cudaError_t launch_attn_causal(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const AttnArgs& args, int grid, cudaStream_t stream);
 
-// Packed variable-length sequences (causal or not): tiles of vt run whole in the
-// listed order; args.B = 1, args.S = T, args.units = vt.n_tiles * H.
+// Packed variable-length sequences, bidirectional: tiles of vt run whole in the
+// listed order; args.B = 1, args.S = T, args.units = vt.n_tiles * H.  (The
+// causal packed form runs as one launch_attn_causal per sequence, with
+// args.epi.row0 = the sequence's first packed row.)
 template <int D>
 cudaError_t launch_attn_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const AttnArgs& args, const VarlenTable& vt, bool causal, int grid,
-                               cudaStream_t stream);
+                               const AttnArgs& args, const VarlenTable& vt, int grid, cudaStream_t stream);
 
 // The same kernel reading Q, K, V from P sequence shards (args.in_Sl = S / P).
 template <int D>

@@ -69,7 +69,8 @@ enum {
     XS_ERR_DEVICE_DRAIN = -14,   /* after an expired wait, a copy or MMA may still have
                                     been in flight when a CTA freed its tensor memory   */
     XS_ERR_DEVICE_BOUNDS = -15,  /* a kernel's index check failed; the access was skipped */
-    XS_ERR_UNAVAILABLE = -16     /* this variant is disabled in this build (see its entry) */
+    XS_ERR_UNAVAILABLE = -16     /* reserved for a variant disabled in a build; no entry
+                                    point of this build returns it                      */
 };
 
 /* Output layouts of xs_attn_fwd_balanced (the three layouts of the entry points
@@ -352,13 +353,16 @@ int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, 
  *   seqlens   HOST int array of n_seqs lengths, each >= 0 (empty sequences are
  *             skipped), read before the call returns.
  *   n_seqs    1 .. 1024.
- *   causal    0: attend to the whole sequence.  Any other value asks for the
- *             causal form, which this build refuses with XS_ERR_UNAVAILABLE
- *             before touching any CUDA state: at 75,776 packed tokens (four
- *             sequences, 40 heads) its launch ended in an unspecified launch
- *             failure, the cause of which is not established, so it is not
- *             launched at all.  (Causal attention over one [B, S, H, D] tensor
- *             is xs_attn_causal_fwd.)
+ *   causal    0: attend to the whole sequence, in one launch over all the
+ *             sequences' tiles.  Any other value: the causal form, run as one
+ *             launch of the causal kernel (xs_attn_causal_fwd's) per non-empty
+ *             sequence, each reading that sequence's rows and storing its row s
+ *             at packed row c_i + s of the layout.  (A single launch over all
+ *             sequences' causal tiles ended, at 75,776 packed tokens in four
+ *             sequences with 40 heads, in an unspecified launch failure whose
+ *             cause is not established; that form is not launched.)  Each
+ *             launch is a separate kernel, so many short sequences pay one
+ *             launch each.
  *   layout    XS_LAYOUT_A2A: outs = P sequence shards [T/P, H, D] of the packed
  *             rows (shard p holds rows [p*T/P, (p+1)*T/P), whichever sequences
  *             they belong to; T % P == 0 and H % P == 0);
@@ -371,9 +375,8 @@ int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, 
  * bit-identical to xs_attn_a2a_fwd on the [B, S, H, D] view of the same memory.
  * Returns XS_OK; XS_ERR_NULL (q, k, v, outs, an out pointer or seqlens);
  * XS_ERR_SHAPE (n_seqs out of range, a negative or too long length, lengths not
- * summing to T, too many tiles or tiles x H, H < 1); XS_ERR_UNAVAILABLE (causal);
- * the checks of xs_attn_a2a_fwd otherwise (with B = 1, S = T); asynchronous on
- * `stream`.
+ * summing to T, too many tiles or tiles x H, H < 1); the checks of
+ * xs_attn_a2a_fwd otherwise (with B = 1, S = T); asynchronous on `stream`.
  */
 int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* seqlens, int n_seqs,
                        int causal, int layout, void* const* outs, int T, int H, int D, int P, float scale,

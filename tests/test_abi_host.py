@@ -202,9 +202,13 @@ def test_varlen_validation(xs):
     # 1024 one-row sequences are 1024 tiles; with 2**21 + 1 heads the work units
     # (tiles x heads) would overflow an int although the dense-shape limits hold
     assert call([1] * 1024, layout=CONT, P=1, H=2 ** 21 + 1, D=64) == xs.XS_ERR_SHAPE
-    # the causal form is disabled: refused on the host, for any otherwise valid call
-    assert call([100, 156], causal=1) == xs.XS_ERR_UNAVAILABLE
-    assert call([256], causal=7, layout=CONT, P=1) == xs.XS_ERR_UNAVAILABLE
+    # the causal form (one causal launch per sequence) takes the same host checks,
+    # and a valid call gets as far as the non-causal one (no GPU here)
+    assert call([100, 155], causal=1) == xs.XS_ERR_DIVISIBILITY
+    assert call([100, 156], causal=1, D=96) == xs.XS_ERR_HEAD_DIM
+    assert call([100, 156], causal=1, q=Q + 8) == xs.XS_ERR_ALIGNMENT
+    assert call([100, 156], causal=1) == call([100, 156])
+    assert call([256], causal=7, layout=CONT, P=1) == call([256], layout=CONT, P=1)
 
 
 def test_workspace_query_validation(xs):
