@@ -4,9 +4,10 @@ protocol, on host models (`_pipeline_model.py`) of what every role walks.
 Schedule: for the shapes the benchmark and the tests launch (and the SM counts
 of other parts), every (tile, key block) is covered exactly once, the balanced
 schedule splits the tiles its definition says it splits, and every TMA row and
-destination row lies inside its tensor.  This includes the packed causal call
-that faulted the GPU (75,776 tokens as four sequences, 40 heads), which the
-library now refuses: its schedule is in range on every CTA.
+destination row lies inside its tensor.  This includes the single-launch
+packed causal schedule whose launch faulted the GPU (75,776 tokens as four
+sequences, 40 heads; the library now runs that form as one causal launch per
+sequence): its schedule is in range on every CTA.
 
 Protocol: one CTA's producer, S issuer, PV issuer and eight softmax warps run
 against phase-counting mbarriers with random timing over the per-CTA piece
