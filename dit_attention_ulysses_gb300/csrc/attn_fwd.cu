@@ -1,4 +1,8 @@
-// Fused non-causal attention + post-attention Ulysses All-to-All store, sm_103a.
+// Fused attention + post-attention Ulysses All-to-All store, sm_103a: the
+// bidirectional kernel (one [B, S, H, D] tensor per operand, or the P sequence
+// shards of the Ulysses ranks), the causal kernel, and the packed-sequence
+// kernel (bidirectional; the causal packed form runs as one causal launch per
+// sequence, with the output row offset EpiParams::row0).
 //
 // X-Stage (arXiv 2607.23264), abstract and the gist.science technical summary,
 // "Key Contributions" item 3 (FlashAttention-A2A piggybacking): the role that
@@ -22,8 +26,8 @@
 //   warp 11    TMA producer (one lane): Q tile of each piece of work, then the
 //              K/V ring in consumption order K0, K1, V0, K2, V1, K3, ...
 //              (D = 128: one Q buffer, reloaded as soon as the piece's last S MMA
-//              has read it, the next one prefetched into L2 meanwhile; D = 64:
-//              two Q buffers)
+//              has read it, the next one prefetched into L2 meanwhile, and 4 ring
+//              stages of 32 KB; D = 64: two Q buffers and 10 stages of 16 KB)
 // The tcgen05 issue queue is shallow, so any control work an issuing thread
 // does between MMAs (waits, commits) leaves the tensor core idle; with two
 // issuers, one thread's control work overlaps the other thread's MMAs.  The
