@@ -373,6 +373,9 @@ def run_ours(args, rank, world, local_rank):
     def varlen():
         xs.xs_attn_varlen_fwd(q_p, k_p, v_p, seqlens, xs.XS_LAYOUT_A2A, varlen_out, w.scale, False, stream)
 
+    def varlen_causal():   # one causal launch per sequence
+        xs.xs_attn_varlen_fwd(q_p, k_p, v_p, seqlens, xs.XS_LAYOUT_A2A, varlen_out, w.scale, True, stream)
+
     for _ in range(max(3, args.warmup)):
         fused()
     torch.cuda.synchronize()
@@ -403,16 +406,17 @@ def run_ours(args, rank, world, local_rank):
     # ablation: attention alone (contiguous store), fused, and attention + separate
     # re-layout, interleaved run by run so that clock drift affects all three alike
     n_abl = max(10, min(args.steps, 50))
-    for fn in (alone, serial_path, causal, varlen) + ((ulysses_fused, ulysses_serial) if uly else ()):
+    for fn in (alone, serial_path, causal, varlen, varlen_causal) + ((ulysses_fused, ulysses_serial) if uly else ()):
         for _ in range(3):
             fn()
-    ta, tf, ts, tc, tv, tuf, tus = [], [], [], [], [], [], []
+    ta, tf, ts, tc, tv, tvc, tuf, tus = [], [], [], [], [], [], [], []
     for _ in range(n_abl):
         ta += time_steps(torch, alone, 1, flush, stream)
         tf += time_steps(torch, fused, 1, flush, stream)
         ts += time_steps(torch, serial_path, 1, flush, stream)
         tc += time_steps(torch, causal, 1, flush, stream)
         tv += time_steps(torch, varlen, 1, flush, stream)
+        tvc += time_steps(torch, varlen_causal, 1, flush, stream)
         if uly:
             tuf += time_steps(torch, ulysses_fused, 1, flush, stream)
             tus += time_steps(torch, ulysses_serial, 1, flush, stream)
@@ -429,6 +433,14 @@ def run_ours(args, rank, world, local_rank):
                    "tflops": varlen_flops / (t_varlen * 1e-3) / 1e12, "flops": varlen_flops,
                    "flops_rule": "4*H*D*sum(len^2) (each sequence attends to itself)",
                    "runs": n_abl, "statistic": "median"}
+    varlen_causal_flops = 2 * H * D * sum(n * (n + 1) for n in seqlens)
+    t_varlen_causal = statistics.median(tvc)
+    varlen_causal_line = {"api": "xs_attn_varlen_fwd(causal=1)", "ms": t_varlen_causal,
+                          "tflops": varlen_causal_flops / (t_varlen_causal * 1e-3) / 1e12,
+                          "flops": varlen_causal_flops,
+                          "flops_rule": "4*H*D*sum(len*(len+1)/2) (unmasked query-key pairs)",
+                          "launches_per_call": sum(1 for n in seqlens if n > 0),
+                          "runs": n_abl, "statistic": "median"}
     ulysses = None
     if uly:
         t_uf, t_us = statistics.median(tuf), statistics.median(tus)
@@ -493,6 +505,7 @@ def run_ours(args, rank, world, local_rank):
         "ulysses_step": ulysses,
         "causal": causal_line,
         "varlen": varlen_line,
+        "varlen_causal": varlen_causal_line,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),
