@@ -71,6 +71,22 @@ def _read_summary(path):
     return vals
 
 
+# ex2.approx.ftz.f32 retired per SM clock per SM on GB300 with two warps per
+# sub-partition (a probe issuing independent ex2 back to back measured 4.12 cycles
+# per warp instruction per sub-partition: 4 x 32 / 4.12 = 31.1).
+MUFU_EX2_PER_CLK_SM = 31.1
+
+
+def mufu_bound(w, sm_mhz, sms):
+    """The attainable rate if the B*H*S^2 exponentials (one per score, 4*D tensor
+    FLOPs each) were the only limit, at the SM clock seen in the timed region."""
+    if not sm_mhz:
+        return None
+    per_s = MUFU_EX2_PER_CLK_SM * sms * sm_mhz * 1e6
+    return {"ex2_per_clk_per_sm": MUFU_EX2_PER_CLK_SM, "sm_mhz": sm_mhz,
+            "bound_tflops": per_s * 4 * w.D / 1e12, "exps_per_step": w.B * w.H * w.S * w.S}
+
+
 def tiles_of(w) -> int:
     return w.B * w.H * ((w.S + 127) // 128)
 
@@ -493,7 +509,12 @@ def run_ours(args, rank, world, local_rank):
                      "peak_kind": f"{peak_kind} bf16 burst",
                      "traffic": traffic,
                      "traffic_source": traffic_note,
-                     "algorithmic_bytes": 4 * w.tensor_bytes},
+                     "algorithmic_bytes": 4 * w.tensor_bytes,
+                     "mufu_bound": mufu_bound(w, (clocks or {}).get("sm_mhz"),
+                                              torch.cuda.get_device_properties(dev).multi_processor_count)},
+        "epilogue_store": {"bytes_per_step": w.tensor_bytes,
+                           "gb_per_s": w.tensor_bytes / (ms_per_step * 1e-3) / 1e9,
+                           "note": "output bytes stored by the fused epilogue over the step time"},
         "overhead_pct": 100.0 * (t_fused - t_alone) / t_alone,
         "ablation": {"attention_alone_ms": t_alone, "fused_ms": t_fused, "attention_plus_relayout_ms": t_serial,
                      "serial_over_fused": t_serial / t_fused, "runs": n_abl, "statistic": "median",
