@@ -640,23 +640,56 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
         // established).  The causal packed call runs as one causal launch per
         // sequence instead: the sequence's rows of Q, K and V as [1, len, H, D]
         // tensors, its output row s stored at packed row start + s of the layout.
+        // A sequence whose launch fills every SM runs on `stream`, one after the
+        // other (concurrent long launches interleave their CTAs and share less
+        // K/V in L2: measured 4 % slower); the shorter ones run on the library's
+        // two side streams (forked from and joined back to `stream`), so that
+        // they fill the SMs the long launches leave idle at their ends.
         const size_t row_bytes = static_cast<size_t>(H) * D * 2;
         const cudaStream_t st = static_cast<cudaStream_t>(stream);
-        int start = 0;
-        for (int i = 0; i < n_seqs; ++i) {
-            const int L = seqlens[i];
-            if (L > 0) {
-                xs::EpiParams es = epi;
-                es.row0 = start;
-                const size_t off = static_cast<size_t>(start) * row_bytes;
-                rc = run_attention(static_cast<const char*>(q) + off, static_cast<const char*>(k) + off,
-                                   static_cast<const char*>(v) + off, nullptr, 0, es, 1, L, H, D, scale, nullptr, 0,
-                                   st, true);
-                if (rc != XS_OK) return rc;
-            }
-            start += L;
+        int starts[xs::MAX_VARLEN_SEQS], order[xs::MAX_VARLEN_SEQS], n_live = 0;
+        for (int i = 0, start = 0; i < n_seqs; start += seqlens[i], ++i) {
+            starts[i] = start;
+            if (seqlens[i] > 0) order[n_live++] = i;
         }
-        return XS_OK;
+        std::stable_sort(order, order + n_live, [&](int x, int y) { return seqlens[x] > seqlens[y]; });
+        auto launch = [&](int i, cudaStream_t s) {
+            xs::EpiParams es = epi;
+            es.row0 = starts[i];
+            const size_t off = static_cast<size_t>(starts[i]) * row_bytes;
+            return run_attention(static_cast<const char*>(q) + off, static_cast<const char*>(k) + off,
+                                 static_cast<const char*>(v) + off, nullptr, 0, es, 1, seqlens[i], H, D, scale,
+                                 nullptr, 0, s, true);
+        };
+        if (n_live == 1) return launch(order[0], st);
+        DeviceInfo dev;
+        if ((rc = device_info(&dev)) != XS_OK) return rc;
+        PipeStreams* ps = nullptr;
+        if ((rc = pipe_streams(&ps)) != XS_OK) return rc;
+        std::lock_guard<std::mutex> lock(ps->mutex);
+        const cudaStream_t lanes[2] = {ps->in, ps->out};
+        cudaError_t e = cudaEventRecord(ps->start, st);
+        for (int j = 0; j < 2 && e == cudaSuccess; ++j) e = cudaStreamWaitEvent(lanes[j], ps->start, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+        double work[2] = {0.0, 0.0};
+        for (int n = 0; n < n_live; ++n) {
+            const int i = order[n];
+            const int64_t units = static_cast<int64_t>((seqlens[i] + 127) / 128) * H;
+            if (units >= dev.sms) {
+                rc = launch(i, st);
+            } else {
+                const int j = work[1] < work[0] ? 1 : 0;
+                work[j] += static_cast<double>(seqlens[i]) * (seqlens[i] + 1);
+                rc = launch(i, lanes[j]);
+            }
+            if (rc != XS_OK) break;
+        }
+        // join even after a failed launch, so that `stream` stays ordered after what was queued
+        for (int j = 0; j < 2; ++j) {
+            if ((e = cudaEventRecord(ps->kernel_done[j], lanes[j])) != cudaSuccess) return cuda_fail(e);
+            if ((e = cudaStreamWaitEvent(st, ps->kernel_done[j], 0)) != cudaSuccess) return cuda_fail(e);
+        }
+        return rc;
     }
     DeviceInfo dev;
     if ((rc = device_info(&dev)) != XS_OK) return rc;

@@ -362,7 +362,11 @@ int xs_attn_causal_fwd(const void* q, const void* k, const void* v, int layout, 
  *             sequences with 40 heads, in an unspecified launch failure whose
  *             cause is not established; that form is not launched.)  Each
  *             launch is a separate kernel, so many short sequences pay one
- *             launch each.
+ *             launch each.  Sequences whose launch fills every SM run on
+ *             `stream` one after the other; shorter ones run on the two library
+ *             streams of xs_attn_a2a_fwd_staged (forked from and joined back to
+ *             `stream`), so that they fill the SMs the long launches leave idle;
+ *             the call stays ordered on `stream`.
  *   layout    XS_LAYOUT_A2A: outs = P sequence shards [T/P, H, D] of the packed
  *             rows (shard p holds rows [p*T/P, (p+1)*T/P), whichever sequences
  *             they belong to; T % P == 0 and H % P == 0);
