@@ -13,8 +13,9 @@ Protocol: `run_cta` plays one CTA's roles (TMA producer, the S = QK^T issuer, th
 O += PV issuer and the eight softmax warps) against mbarriers with phase
 counters, the tensor pipe completing MMAs in issue order and TMA copies landing
 in any order, with random timing.  Every wait states the phase it means; the
-model asserts that the parity the kernel would wait on names that phase, that no
-later phase of the same barrier has completed by then (the parity would alias),
+model asserts that the parity the kernel would wait on names that phase, that
+neither a later phase has completed nor an earlier one is still open when the
+wait starts (either way the parity would alias),
 that no buffer is overwritten before its reader is done, and that the roles
 finish (no deadlock).  The barrier layout follows the kernel: Q_FULL/Q_FREE per
 Q buffer, S_FULL/P_FULL/P_FREE per score buffer (three; P is written over the
@@ -181,11 +182,13 @@ MUTATIONS = ("skip_buffer_wait", "two_buffer_parity", "skip_o_final_wait", "skip
              "skip_kv_free_wait", "early_p_signal")
 
 
-def run_cta(piece_blocks, D=128, seed=0, rescale_rate=0.25, mutate=None):
+def run_cta(piece_blocks, D=128, seed=0, rescale_rate=0.25, mutate=None, stall=0.85):
     """Play one CTA over pieces of the given key-block counts; raises on a
     parity alias, a buffer hazard or a deadlock.  Returns the number of steps.
     `mutate` plants one of MUTATIONS (a wait left out or a wrong parity), so
-    that the tests can show the model catches it."""
+    that the tests can show the model catches it.  Each role skips a scheduling
+    round with a probability of its own, drawn from [0, stall) per run (some
+    warps fall well behind the others)."""
     assert mutate is None or mutate in MUTATIONS
     rnd = random.Random(seed)
     QB, NS = cfg(D)
@@ -225,6 +228,8 @@ def run_cta(piece_blocks, D=128, seed=0, rescale_rate=0.25, mutate=None):
     def wait(bar, parity, phase):
         if parity != (phase & 1):
             raise ProtocolError(f"{bar.name}: parity {parity} does not name phase {phase}")
+        if bar.done < phase:
+            raise ProtocolError(f"{bar.name}: wait for phase {phase} starts while phase {bar.done} is open")
         return ("wait", bar, phase)
 
     def producer():
@@ -386,6 +391,7 @@ def run_cta(piece_blocks, D=128, seed=0, rescale_rate=0.25, mutate=None):
     for w in range(SOFTMAX_WARPS):
         roles[f"softmax{w}"] = softmax(w)
     blocked = {r: None for r in roles}
+    p_stall = {r: rnd.uniform(0.0, stall) for r in roles}
     alive = set(roles)
     steps = 0
     while alive:
@@ -394,6 +400,9 @@ def run_cta(piece_blocks, D=128, seed=0, rescale_rate=0.25, mutate=None):
         order = sorted(alive)
         rnd.shuffle(order)
         for r in order:
+            if rnd.random() < p_stall[r]:
+                progressed = True
+                continue
             bw = blocked[r]
             if bw is not None:
                 _, bar, k = bw
