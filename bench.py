@@ -34,6 +34,7 @@ import dit_inputs as di  # noqa: E402
 
 DEFAULT_WORKLOAD = "video_large"
 SIDE_WORKLOAD = "image"   # timed as an extra key of the default line
+D64_WORKLOAD = "video_small_d64"   # the head-dimension-64 kernel, another extra key
 METRIC = "fused attn+A2A-layout TFLOP/s and % of GB300 dense BF16 peak; fused-store overhead %"
 KERNEL_SOURCES = ["dit_attention_ulysses_gb300/csrc/attn_fwd.cu", "dit_attention_ulysses_gb300/csrc/ptx.cuh",
                   "dit_attention_ulysses_gb300/csrc/kernels.h"]
@@ -104,7 +105,7 @@ def ncu_traffic(w):
         names.insert(0, own)
     for name in names:
         vals = _read_summary(os.path.join(PROFILES, name))
-        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        if vals.get("kernel_source_sha256_16") != kernel_source_hash() or vals.get("head_dim", "128") != str(w.D):
             continue
         try:
             if vals.get("workload") == w.name:
@@ -299,10 +300,10 @@ def varlen_mix(total: int, seed: int = 12345):
     return lens
 
 
-def side_workload_line(torch, xs, args, dev, stream, flush):
-    """The fused call on the image-DiT workload, timed like the main line (L2 flushed
-    before each step), reported beside it."""
-    w = di.WORKLOADS[SIDE_WORKLOAD]
+def side_workload_line(torch, xs, args, dev, stream, flush, name=SIDE_WORKLOAD):
+    """The fused call on another workload (the image-DiT shape, the D = 64 kernel),
+    timed like the main line (L2 flushed before each step), reported beside it."""
+    w = di.WORKLOADS[name]
     q, k, v = (to_device(x, torch, dev) for x in di.random_qkv(w))
     outs = [torch.empty((w.B, w.S // w.P, w.H, w.D), dtype=torch.bfloat16, device=dev) for _ in range(w.P)]
     ws = xs.Workspace.for_shape(w.B, w.S, w.H, w.D, device=dev) if args.schedule == "balanced" else None
@@ -313,8 +314,11 @@ def side_workload_line(torch, xs, args, dev, stream, flush):
     ms = time_steps(torch, fn, n, flush, stream)
     if xs.xs_attn_get_device_error(stream) != 0:
         raise RuntimeError("device error in the side workload")
+    tflops = w.flops / (statistics.mean(ms) * 1e-3) / 1e12
+    peak = measured_peaks()[0]
     return {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "P": w.P, "steps": n,
-            "ms_per_step": statistics.mean(ms), "tflops": w.flops / (statistics.mean(ms) * 1e-3) / 1e12,
+            "ms_per_step": statistics.mean(ms), "tflops": tflops,
+            "frac_of_bf16_burst": tflops / peak if peak else None,
             "step_ms_percentiles": step_percentiles(ms), "api": "xs_attn_fwd_balanced"}
 
 
@@ -479,6 +483,7 @@ def run_ours(args, rank, world, local_rank):
     if xs.xs_attn_get_device_error(stream) != 0:
         raise RuntimeError("device error after ablation / e2e runs")
     side = side_workload_line(torch, xs, args, dev, stream, flush) if args.workload != SIDE_WORKLOAD else None
+    d64 = side_workload_line(torch, xs, args, dev, stream, flush, D64_WORKLOAD) if w.D != 64 else None
 
     if rank != 0:
         return
@@ -533,6 +538,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if side is not None:
         line["side_workload"] = side
+    if d64 is not None:
+        line["d64_workload"] = d64
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"], (rb, rs, ref) = cpu_oracle_sample(w, seconds_target=args.cpu_seconds,
                                                                 inputs=(qb, kb, vb))

@@ -86,6 +86,10 @@ WORKLOADS = {
     "video_large": Workload("video_large", B=1, H=40, S=75776, D=128, P=8,
                             scale=1.0 / math.sqrt(128), outliers=4,
                             note="video-DiT large with outlier channels, 8 shards of [1,9472,40,128]"),
+    # head dimension 64 at the small video model's width (24 x 64 = 12 x 128)
+    "video_small_d64": Workload("video_small_d64", B=1, H=24, S=32768, D=64, P=4,
+                                scale=1.0 / math.sqrt(64),
+                                note="video-DiT small, 24 heads of 64, 4 shards of [1,8192,24,64]"),
 }
 for _s in SWEEP_S:
     WORKLOADS[f"sweep_S{_s}"] = sweep_workload(_s)
@@ -149,10 +153,22 @@ def random_qkv(w: Workload, S: int | None = None):
 # exact in bf16.
 # ----------------------------------------------------------------------------
 LAYOUT_REP = 7
+LAYOUT_REP_MIN = 4   # where 7 repeats per bit do not fit D (long sequences at D = 64)
 
 
 def _layout_nbits(S: int) -> int:
     return max(1, math.ceil(math.log2(S))) if S > 1 else 1
+
+
+def _layout_rep(S: int, D: int) -> int:
+    """Channels per code bit: 7 where they fit, else 4 (the own key then beats
+    every other by at least 8 in q.k, and the second-best weight is exp(-16*8)
+    relative to it, still far below fp32 resolution)."""
+    nbits = _layout_nbits(S)
+    for r in (LAYOUT_REP, LAYOUT_REP_MIN):
+        if nbits * r <= D:
+            return r
+    raise ValueError(f"S={S} needs {nbits * LAYOUT_REP_MIN} code channels > D={D}")
 
 
 def layout_code_value(b: int, s: np.ndarray | int, h: int, D: int) -> np.ndarray:
@@ -170,18 +186,18 @@ def layout_code_value(b: int, s: np.ndarray | int, h: int, D: int) -> np.ndarray
 def layout_code_inputs(B: int, S: int, H: int, D: int):
     """(q, k, v, scale) bf16 bit arrays for the one-hot layout test.
 
-    Requires ceil(log2 S) * 7 <= D, i.e. S <= 2**18 at D = 128 and S <= 2**9
-    at D = 64.  The returned scale (16) makes the second-best key's weight
-    exp(-16*14) relative to the own key, far below fp32 resolution.
+    Each bit of s takes 7 channels where ceil(log2 S) * 7 <= D (S <= 2**18 at
+    D = 128, S <= 2**9 at D = 64), else 4 (S <= 2**16 at D = 64).  The returned
+    scale (16) makes the second-best key's weight exp(-16*14), or exp(-16*8)
+    with 4 channels per bit, relative to the own key: far below fp32 resolution.
     """
     nbits = _layout_nbits(S)
-    if nbits * LAYOUT_REP > D:
-        raise ValueError(f"S={S} needs {nbits * LAYOUT_REP} code channels > D={D}")
+    r = _layout_rep(S, D)
     s = np.arange(S)
     code = np.ones((S, D), dtype=np.float32)
     for i in range(nbits):
         bit = ((s >> i) & 1).astype(np.float32) * 2.0 - 1.0
-        code[:, i * LAYOUT_REP:(i + 1) * LAYOUT_REP] = bit[:, None]
+        code[:, i * r:(i + 1) * r] = bit[:, None]
     qk = np.broadcast_to(code[None, :, None, :], (B, S, H, D))
     q = f32_to_bf16_bits(qk)
     k = q.copy()
@@ -227,13 +243,12 @@ def layout_code_inputs_torch(B: int, S: int, H: int, D: int, device="cuda"):
     below 256."""
     import torch
     nbits = _layout_nbits(S)
-    if nbits * LAYOUT_REP > D:
-        raise ValueError(f"S={S} needs {nbits * LAYOUT_REP} code channels > D={D}")
+    r = _layout_rep(S, D)
     s = torch.arange(S, device=device, dtype=torch.int64)
     code = torch.ones((S, D), device=device, dtype=torch.float32)
     for i in range(nbits):
         bit = ((s >> i) & 1).to(torch.float32) * 2.0 - 1.0
-        code[:, i * LAYOUT_REP:(i + 1) * LAYOUT_REP] = bit[:, None]
+        code[:, i * r:(i + 1) * r] = bit[:, None]
     q = code.to(torch.bfloat16)[None, :, None, :].expand(B, S, H, D).contiguous()
     k = q.clone()
     v = layout_code_value_torch(B, S, H, D, device)

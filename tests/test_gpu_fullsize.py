@@ -13,9 +13,10 @@ from _parity import abs_bits, assert_close, bits_to_torch, torch_to_f64
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-FULL = ["tiny", "image", "video_small", "video_large", "sweep_S1024", "sweep_S8192", "sweep_S131072"]
+FULL = ["tiny", "image", "video_small", "video_large", "sweep_S1024", "sweep_S8192", "sweep_S131072",
+        "video_small_d64"]
 ROWS = {"tiny": 256, "image": 192, "video_small": 96, "video_large": 48,
-        "sweep_S1024": 128, "sweep_S8192": 96, "sweep_S131072": 24}
+        "sweep_S1024": 128, "sweep_S8192": 96, "sweep_S131072": 24, "video_small_d64": 96}
 
 
 @pytest.fixture(scope="module")
@@ -63,7 +64,7 @@ def test_random_sampled_rows_full(xs, name):
     assert_close(got, ref, mass, name)
 
 
-@pytest.mark.parametrize("name", ["video_large", "sweep_S131072"])
+@pytest.mark.parametrize("name", ["video_large", "sweep_S131072", "video_small_d64"])
 def test_balanced_split_schedule_sampled_rows_full(xs, name):
     """The launch the benchmark times at these shapes: xs_attn_fwd_balanced with
     its workspace, whose leftover tiles are cut among CTAs and merged in the

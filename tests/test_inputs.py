@@ -1,4 +1,6 @@
 """The seeded input generators: reproducible, correctly rounded, right shapes."""
+import math
+
 import numpy as np
 import pytest
 
@@ -41,7 +43,7 @@ def test_outlier_channels_scaled():
             assert np.all(std[mask] > 6) and np.all(std[~mask] < 1.2)
 
 
-@pytest.mark.parametrize("S,D", [(256, 64), (1000, 128), (75776, 128)])
+@pytest.mark.parametrize("S,D", [(256, 64), (1000, 128), (75776, 128), (1024, 64), (32768, 64)])
 def test_layout_code_dot_products(S, D):
     q, k, v, scale = di.layout_code_inputs(1, S, 1, D)
     qf = di.bf16_bits_to_f32(q)[0, :, 0, :].astype(np.float64)
@@ -50,7 +52,8 @@ def test_layout_code_dot_products(S, D):
     t = rng.integers(0, S, 64)
     dots = (qf[s] * qf[t]).sum(axis=1)
     ham = np.array([bin(int(a) ^ int(b)).count("1") for a, b in zip(s, t)])
-    np.testing.assert_array_equal(dots, D - 14 * ham)
+    r = 7 if math.ceil(math.log2(S)) * 7 <= D else 4   # channels per bit
+    np.testing.assert_array_equal(dots, D - 2 * r * ham)
     vf = di.bf16_bits_to_f32(v)[0, :, 0, :]
     np.testing.assert_array_equal(vf[s], di.layout_code_value(0, s, 0, D))
 

@@ -140,16 +140,18 @@ def test_scale_zero_gives_mean_of_v():
     np.testing.assert_allclose(got, np.broadcast_to(mean, got.shape), rtol=1e-12, atol=1e-14)
 
 
-@pytest.mark.parametrize("B,S,H,D", [(1, 256, 2, 64), (2, 96, 4, 64), (1, 1000, 2, 128)])
+@pytest.mark.parametrize("B,S,H,D", [(1, 256, 2, 64), (2, 96, 4, 64), (1, 1000, 2, 128), (1, 1024, 1, 64)])
 def test_one_hot_rows_copy_own_value_row(B, S, H, D):
     """Index-coded Q = K with a large scale: every row's softmax is one-hot on
-    its own key, so O = V exactly (the expected value is the encoding itself)."""
+    its own key, so O = V exactly (the expected value is the encoding itself).
+    S = 1024 at D = 64 takes the code with 4 channels per bit."""
     q, k, v, scale = di.layout_code_inputs(B, S, H, D)
     got = oracle.attention(q, k, v, scale)
-    # every other key trails the own key by >= 14 in q.k, so its weight is
-    # <= exp(-14*scale); with values < 256 the exact output differs from the
-    # own value row by less than S * 256 * exp(-14*scale)
-    bound = S * 256 * math.exp(-14 * scale)
+    # every other key trails the own key by >= 2 * (channels per bit) in q.k, so
+    # its weight is <= exp(-gap*scale); with values < 256 the exact output differs
+    # from the own value row by less than S * 256 * exp(-gap*scale)
+    gap = 14 if math.ceil(math.log2(S)) * 7 <= D else 8
+    bound = S * 256 * math.exp(-gap * scale)
     for b in range(B):
         for h in range(H):
             np.testing.assert_allclose(got[b, :, h, :],
