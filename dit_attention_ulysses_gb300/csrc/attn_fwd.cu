@@ -290,10 +290,9 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
 }
 
 __device__ __forceinline__ void decode_unit(int u, const AttnArgs& a, int& b, int& h, int& qt) {
-    qt = u % a.n_qt;
-    const int bh = u / a.n_qt;
-    h = bh % a.H;
-    b = bh / a.H;
+    int bh;
+    fdivmod(u, a.fd_nqt, bh, qt);
+    fdivmod(bh, a.fd_H, b, h);
 }
 
 // One piece of work of a CTA: key blocks [k0, k0 + nb) of query tile (b, h, qt).
@@ -349,7 +348,7 @@ __device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* v
     if constexpr (VARLEN) {
         const long long u = static_cast<long long>(idx) * G + ((idx & 1) ? G - 1 - i : i);
         if (u >= a.units) return false;
-        const int t = static_cast<int>(u) / a.H;
+        const int t = fdiv(static_cast<int>(u), a.fd_H);
         // index checks on the host-built table (every role takes the same exit)
         if (t >= vt->n_tiles) {
             report_error(XS_DEVICE_BOUNDS_CODE, 1, t, vt->n_tiles, idx);
@@ -388,17 +387,15 @@ __device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* v
         const long long u = static_cast<long long>(idx) * G + ((idx & 1) ? G - 1 - i : i);
         if (u >= a.units) return false;
         const int t = static_cast<int>(u);
-        int bh;
+        int bh, r;
         if (a.causal_head_major) {
-            bh = t / a.n_qt;
-            w.qt = a.n_qt - 1 - (t - bh * a.n_qt);
+            fdivmod(t, a.fd_nqt, bh, r);     // r: position within the head, longest first
+            w.qt = a.n_qt - 1 - r;
         } else {
-            const int bhs = a.B * a.H;
-            bh = t % bhs;
-            w.qt = a.n_qt - 1 - t / bhs;
+            fdivmod(t, a.fd_BH, r, bh);      // r: rank of the query tile, longest first
+            w.qt = a.n_qt - 1 - r;
         }
-        w.h = bh % a.H;
-        w.b = bh / a.H;
+        fdivmod(bh, a.fd_H, w.b, w.h);
         w.k0 = 0;
         w.nb = w.qt + 1;
         w.kind = WORK_FULL;
@@ -407,7 +404,7 @@ __device__ __forceinline__ bool get_work(const AttnArgs& a, const VarlenTable* v
     }
     const int n = a.n_kv;
     const int dp = a.sp.dp_tiles;
-    const int ndp = dp > i ? (dp - i + G - 1) / G : 0;
+    const int ndp = dp > i ? fdiv(dp - i + G - 1, a.fd_grid) : 0;
     int tile, k0 = 0, k1 = n;
     if (idx < ndp) {
         tile = i + idx * G;
@@ -804,11 +801,13 @@ __device__ __noinline__ bool split_epilogue(const AttnArgs& a, const Work& w, ui
     __nv_bfloat16* dst = nullptr;
     if (store) {
         const int hg = a.h0_out + w.h;   // head in the output layout
-        const int p = s_row / a.epi.Sl + hg / a.epi.Hl;
+        int ps, s_dst, ph, h_dst;
+        fdivmod(s_row, a.epi.fd_Sl, ps, s_dst);
+        fdivmod(hg, a.epi.fd_Hl, ph, h_dst);
+        const int p = ps + ph;
         if (p < MAX_PTRS && a.epi.ptr[p] != nullptr) {
             dst = reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
-                  ((static_cast<size_t>(w.b) * a.epi.Sl + s_row % a.epi.Sl) * a.epi.Hl + hg % a.epi.Hl) * D +
-                  half * DH;
+                  ((static_cast<size_t>(w.b) * a.epi.Sl + s_dst) * a.epi.Hl + h_dst) * D + half * DH;
         } else {
             report_error(XS_DEVICE_BOUNDS_CODE, 2, p, s_row, w.h);
             store = false;
@@ -987,9 +986,10 @@ __device__ void softmax_role(const AttnArgs& a, const VarlenTable* vt, uint8_t* 
             unsigned long long dst_row = 0;   // this lane's half row in the destination (0: past the sequence)
             if (s_loc < (VARLEN ? w.len : a.S)) {
                 const int s_row = (VARLEN ? w.row0 : a.epi.row0) + s_loc;
-                const int p = s_row / a.epi.Sl + h / a.epi.Hl;
-                const int s_dst = s_row % a.epi.Sl;
-                const int h_dst = h % a.epi.Hl;
+                int ps, s_dst, ph, h_dst;
+                fdivmod(s_row, a.epi.fd_Sl, ps, s_dst);
+                fdivmod(h, a.epi.fd_Hl, ph, h_dst);
+                const int p = ps + ph;
                 if (p < MAX_PTRS && a.epi.ptr[p] != nullptr)
                     dst_row = reinterpret_cast<unsigned long long>(
                         reinterpret_cast<__nv_bfloat16*>(a.epi.ptr[p]) +
@@ -1169,6 +1169,19 @@ int attn_smem_bytes() {
     return Cfg<D>::SMEM_ALLOC;
 }
 
+// The arguments with the tile-decode and destination divisors filled in (every
+// launch goes through here, so the kernel never sees stale ones).
+static AttnArgs with_divisors(const AttnArgs& args, int grid) {
+    AttnArgs a = args;
+    a.fd_nqt = make_fastdiv(a.n_qt > 0 ? a.n_qt : 1);
+    a.fd_H = make_fastdiv(a.H > 0 ? a.H : 1);
+    a.fd_BH = make_fastdiv(a.B * a.H > 0 ? a.B * a.H : 1);
+    a.fd_grid = make_fastdiv(grid > 0 ? grid : 1);
+    a.epi.fd_Sl = make_fastdiv(a.epi.Sl > 0 ? a.epi.Sl : 1);
+    a.epi.fd_Hl = make_fastdiv(a.epi.Hl > 0 ? a.epi.Hl : 1);
+    return a;
+}
+
 static_assert(Cfg<128>::SMEM_ALLOC <= 232448, "shared memory budget (D = 128)");
 static_assert(Cfg<64>::SMEM_ALLOC <= 232448, "shared memory budget (D = 64)");
 
@@ -1179,13 +1192,13 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     if (!cooperative) {
-        kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, args);
+        kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, with_divisors(args, grid));
         return cudaGetLastError();
     }
     // CTAs of a split tile wait for each other: all of them must be resident at
     // once, which a cooperative launch guarantees (or refuses to launch).
     CUtensorMap q = tq, k = tk, v = tv;
-    AttnArgs a = args;
+    AttnArgs a = with_divisors(args, grid);
     void* params[] = {&q, &k, &v, &a};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(NUM_THREADS), params,
                                        Cfg<D>::SMEM_ALLOC, stream);
@@ -1199,11 +1212,11 @@ cudaError_t launch_attn_sharded(const ShardMaps& maps, int P, const AttnArgs& ar
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     if (!cooperative) {
-        kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(args, maps);
+        kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(with_divisors(args, grid), maps);
         return cudaGetLastError();
     }
     ShardMaps m = maps;
-    AttnArgs a = args;
+    AttnArgs a = with_divisors(args, grid);
     void* params[] = {&a, &m};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(NUM_THREADS), params,
                                        Cfg<D>::SMEM_ALLOC, stream);
@@ -1215,7 +1228,7 @@ cudaError_t launch_attn_causal(const CUtensorMap& tq, const CUtensorMap& tk, con
     auto kern = attn_causal_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, args);
+    kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, with_divisors(args, grid));
     return cudaGetLastError();
 }
 
@@ -1225,7 +1238,7 @@ cudaError_t launch_attn_varlen(const CUtensorMap& tq, const CUtensorMap& tk, con
     auto kern = attn_varlen_kernel<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, args, vt);
+    kern<<<grid, NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(tq, tk, tv, with_divisors(args, grid), vt);
     return cudaGetLastError();
 }
 

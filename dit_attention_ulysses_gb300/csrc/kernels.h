@@ -24,6 +24,37 @@ struct DeviceErrorInfo {
     int detail[3];  // waits: phase parity, piece index, key block; index checks: the values checked
 };
 
+// Division by a launch-constant divisor d >= 1 without a divide instruction, for
+// dividends 0 <= n < 2^31 (round-up method of division by invariant integers):
+// with l = ceil(log2 d) and m = ceil(2^(31+l) / d) (< 2^32), floor(n / d) =
+// floor(n * m / 2^(31+l)).  The error n*(m*d - 2^(31+l)) / (d * 2^(31+l)) of the
+// product is below 2^-l <= 1/d, too small to reach the next integer.
+struct FastDiv {
+    unsigned m;
+    unsigned shift;   // 31 + l
+    int d;
+};
+
+inline FastDiv make_fastdiv(int d) {
+    FastDiv f{};
+    unsigned l = 0;
+    while ((1ull << l) < static_cast<unsigned long long>(d)) ++l;
+    f.shift = 31 + l;
+    f.m = static_cast<unsigned>(((1ull << f.shift) + static_cast<unsigned long long>(d) - 1) /
+                                static_cast<unsigned long long>(d));
+    f.d = d;
+    return f;
+}
+
+__host__ __device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+    return static_cast<int>((static_cast<unsigned long long>(static_cast<unsigned>(n)) * f.m) >> f.shift);
+}
+// n / d and n % d
+__host__ __device__ __forceinline__ void fdivmod(int n, const FastDiv& f, int& q, int& r) {
+    q = fdiv(n, f);
+    r = n - q * f.d;
+}
+
 // Where each output row (b, s, h) of the attention kernel goes:
 //   p = s / Sl + h / Hl,  ptr[p] + ((b * Sl + s % Sl) * Hl + h % Hl) * D
 // contiguous:   Sl = S,   Hl = H,   one pointer
@@ -34,6 +65,7 @@ struct EpiParams {
     int Sl;
     int Hl;
     int row0;   // output row of the launch's row 0 (one sequence of a packed batch; else 0)
+    FastDiv fd_Sl, fd_Hl;   // set by the launch functions from Sl and Hl
 };
 
 // Balanced ("stream-K") schedule of the tiles left over after the whole waves.
@@ -81,6 +113,8 @@ struct AttnArgs {
     int h0_out;     // ... and head h0_out + h of the output layout (both 0: all heads;
                     // a head group of larger tensors: both the group's first head; a
                     // Ulysses rank r with H/P local heads: 0 and r * H/P)
+    // divisors of the tile decode, set by the launch functions (callers leave them)
+    FastDiv fd_nqt, fd_H, fd_BH, fd_grid;
 };
 
 // Packed variable-length sequences (B = 1, S = T rows in total): the sequence
