@@ -146,8 +146,8 @@ def test_causal_last_row_equals_bidirectional(xs, S):
 
 
 @pytest.mark.parametrize("B,S,H,D,P", [(1, 4608, 24, 128, 4), (1, 4000, 5, 128, 5), (2, 512, 4, 64, 2),
-                                       (1, 75776, 40, 128, 8)],
-                         ids=["image", "ragged_two_waves", "d64", "video_large"])
+                                       (1, 75776, 40, 128, 8), (1, 1040, 16, 64, 16)],
+                         ids=["image", "ragged_two_waves", "d64", "video_large", "p16_sl65"])
 def test_causal_layout_code_bit_exact(xs, B, S, H, D, P):
     """Index-coded inputs: the own key dominates every other by a weight ratio
     below fp32 resolution and lies inside the causal window, so every output

@@ -54,6 +54,9 @@ CASES = [
     ("s129", 1, 129, 2, 128, 1),
     ("s384_p8", 1, 384, 8, 128, 8),
     ("b3_h5", 3, 640, 5, 64, 5),
+    # the most shards the ABI takes (16): 65-row shards, so every 128-row tile is
+    # routed to two or three of them
+    ("p16_sl65", 1, 1040, 16, 64, 16),
 ]
 
 
@@ -84,7 +87,8 @@ def test_outlier_channels_small(xs):
     assert_close(got, ref, mass, "outliers")
 
 
-@pytest.mark.parametrize("B,S,H,D,P", [(1, 256, 2, 64, 2), (2, 1000, 4, 128, 4), (1, 4608, 24, 128, 4)])
+@pytest.mark.parametrize("B,S,H,D,P", [(1, 256, 2, 64, 2), (2, 1000, 4, 128, 4), (1, 4608, 24, 128, 4),
+                                       (1, 1040, 16, 64, 16), (2, 2048, 32, 128, 16)])
 def test_layout_bit_exact(xs, B, S, H, D, P):
     q, k, v, scale = di.layout_code_inputs_torch(B, S, H, D)
     outs = [torch.full((B, S // P, H, D), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
@@ -117,7 +121,8 @@ def test_scale_zero_gives_mean_of_v(xs):
     assert np.abs(got - mean).max() <= 2 ** -8 * np.abs(mean).max() + 1e-6
 
 
-@pytest.mark.parametrize("B,S,H,D,P", [(1, 1024, 8, 128, 4), (2, 600, 6, 64, 3)])
+@pytest.mark.parametrize("B,S,H,D,P", [(1, 1024, 8, 128, 4), (2, 600, 6, 64, 3), (1, 1040, 16, 64, 16),
+                                       (2, 2048, 32, 128, 16)])
 def test_fused_equals_contiguous_and_serial_path(xs, B, S, H, D, P):
     w = di.Workload("abl", B=B, H=H, S=S, D=D, P=P, scale=1 / math.sqrt(D), seed=7)
     q, k, v = (bits_to_torch(x) for x in di.random_qkv(w))

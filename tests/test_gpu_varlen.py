@@ -119,8 +119,9 @@ def test_varlen_layouts_bit_identical(xs):
 
 @pytest.mark.parametrize("causal", [False, True], ids=["bidir", "causal"])
 @pytest.mark.parametrize("seqlens,H,D,P", [([1000, 1, 129, 0, 918], 8, 128, 4),
-                                           ([27916, 12272, 30881, 4707], 40, 128, 8)],
-                         ids=["mix", "video_large_tokens"])
+                                           ([27916, 12272, 30881, 4707], 40, 128, 8),
+                                           ([500, 12, 700, 324], 16, 64, 16)],
+                         ids=["mix", "video_large_tokens", "p16_sl96"])
 def test_varlen_layout_code_bit_exact(xs, seqlens, H, D, P, causal):
     """Index-coded inputs over the packed rows: each row's own key dominates
     every other key of its sequence, so every output row is its own V row.  The
