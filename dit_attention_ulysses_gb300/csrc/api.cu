@@ -664,6 +664,11 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
         if (n_live == 1) return launch(order[0], st);
         DeviceInfo dev;
         if ((rc = device_info(&dev)) != XS_OK) return rc;
+        auto fills_gpu = [&](int i) { return static_cast<int64_t>((seqlens[i] + 127) / 128) * H >= dev.sms; };
+        if (std::all_of(order, order + n_live, fills_gpu)) {   // nothing for the side streams
+            for (int n = 0; n < n_live && rc == XS_OK; ++n) rc = launch(order[n], st);
+            return rc;
+        }
         PipeStreams* ps = nullptr;
         if ((rc = pipe_streams(&ps)) != XS_OK) return rc;
         std::lock_guard<std::mutex> lock(ps->mutex);
@@ -674,8 +679,7 @@ int xs_attn_varlen_fwd(const void* q, const void* k, const void* v, const int* s
         double work[2] = {0.0, 0.0};
         for (int n = 0; n < n_live; ++n) {
             const int i = order[n];
-            const int64_t units = static_cast<int64_t>((seqlens[i] + 127) / 128) * H;
-            if (units >= dev.sms) {
+            if (fills_gpu(i)) {
                 rc = launch(i, st);
             } else {
                 const int j = work[1] < work[0] ? 1 : 0;
