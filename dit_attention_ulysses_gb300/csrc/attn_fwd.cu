@@ -241,6 +241,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return ok;
 }
 
+// Suspend hint of the single-thread roles' probes (ns): a suspended thread is
+// woken by the phase's completion, and while it sleeps it takes no issue slots
+// from the softmax warps on its sub-partition (measured +1 ... +1.4 % at the long
+// power-limited shapes, no change at the short ones, against hint-free probes).
+constexpr uint32_t ROLE_WAIT_HINT_NS = 2000;
+
 // The same bounded wait for a single thread (the issuing lanes of the producer
 // and MMA roles), without warp votes.
 __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -248,7 +254,7 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volat
     if (mbar_test_wait(bar, parity)) return true;
     uint64_t t0 = 0;
     for (uint32_t n = 0;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, ROLE_WAIT_HINT_NS)) return true;
         if ((n & (WAIT_CHECK_EVERY - 1)) != 0) continue;
         if (*abort_flag) return false;
         if (n == 0) t0 = globaltimer_ns();
