@@ -191,14 +191,18 @@ def to_device(bits, torch, dev):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
 
-def time_steps(torch, fn, steps, flush, stream):
-    """Run `steps` timed calls of fn with an L2 flush before each; returns per-step ms list."""
+def time_steps(torch, fn, steps, flush, stream, host_ms=None):
+    """Run `steps` timed calls of fn with an L2 flush before each; returns per-step ms list.
+    `host_ms`, when given, receives the host time each call took to return (enqueue)."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
         flush.add_(1)
         starts[i].record(stream)
+        t0 = time.perf_counter()
         fn()
+        if host_ms is not None:
+            host_ms.append((time.perf_counter() - t0) * 1e3)
         ends[i].record(stream)
     torch.cuda.synchronize()
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -478,7 +482,8 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(2):
         e2e_fn()
     n_e2e = max(3, min(args.steps, 20))
-    e2e_steps = time_steps(torch, e2e_fn, n_e2e, flush, stream)
+    e2e_host = []
+    e2e_steps = time_steps(torch, e2e_fn, n_e2e, flush, stream, host_ms=e2e_host)
     e2e_ms = max_over_ranks(statistics.mean(e2e_steps), world)
     if xs.xs_attn_get_device_error(stream) != 0:
         raise RuntimeError("device error after ablation / e2e runs")
@@ -527,6 +532,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": whole_job_tflops(w.flops, e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 3 * w.tensor_bytes, "d2h_bytes_per_step": w.tensor_bytes,
                 "ms_per_step": e2e_ms, "step_ms_percentiles": step_percentiles(e2e_steps),
+                "step_ms": [round(x, 2) for x in e2e_steps], "host_enqueue_ms": [round(x, 2) for x in e2e_host],
                 "api": "xs_attn_a2a_fwd_staged"},
         "ulysses_step": ulysses,
         "causal": causal_line,
