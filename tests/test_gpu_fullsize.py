@@ -103,3 +103,45 @@ def test_balanced_split_schedule_sampled_rows_full(xs, name):
     above = int((np.abs(got - ref) > 2e-2).sum())
     print(f"{name} balanced: {len(rows)} rows x {w.H} heads x {w.D}: max-abs {max_abs:.4g}, rel-L2 {rel:.3g}, "
           f"{above} of {got.size} elements above 2e-2 ({len(splits)} split tiles)")
+
+
+def test_max_sequence_layout_bit_exact(xs):
+    """The longest sequence the tests run, 2^20 rows (B=1, H=8, D=128, P=8: 2 GB
+    per tensor), index-coded: every output element of every shard is its own V
+    row bit for bit.  Rows, tiles and work units here exceed every size the other
+    tests reach, so any 32-bit overflow in the row, tile or address arithmetic
+    would misplace rows.  The code takes 4 channels per bit of the 20-bit index."""
+    B, S, H, D, P = 1, 1 << 20, 8, 128, 8
+    q, k, v, scale = di.layout_code_inputs_torch(B, S, H, D)
+    outs = _shards(w=di.Workload("max_s", B=B, H=H, S=S, D=D, P=P, scale=scale))
+    xs.xs_attn_a2a_fwd(q, k, v, outs, scale)
+    torch.cuda.synchronize()
+    assert xs.xs_attn_get_device_error() == 0
+    del q, k, v
+    Sl = S // P
+    for p in range(P):
+        exp = di.layout_code_value_torch(B, S, H, D, s_offset=p * Sl, S_rows=Sl)
+        eq = outs[p].view(torch.int16) == exp.view(torch.int16)
+        assert bool(eq.all()), f"shard {p}: {int((~eq).sum())} elements differ"
+        del exp, eq
+
+
+def test_max_sequence_random_sampled_rows(xs):
+    """Random data at 2^20 rows (B=1, H=2, D=64, P=2) on the balanced schedule
+    against the fp64 oracle on 16 seeded rows (every shard's first and last
+    among them), all heads."""
+    import oracle
+    w = di.Workload("max_s_d64", B=1, H=2, S=1 << 20, D=64, P=2, scale=0.125, seed=11)
+    qb, kb, vb = di.random_qkv(w)
+    outs = _shards(w)
+    ws = xs.Workspace(xs.xs_attn_workspace_bytes(w.B, w.S, w.H, w.D))
+    xs.xs_attn_fwd_balanced(bits_to_torch(qb), bits_to_torch(kb), bits_to_torch(vb), xs.XS_LAYOUT_A2A, outs,
+                            w.scale, ws)
+    torch.cuda.synchronize()
+    assert xs.xs_attn_get_device_error() == 0
+    rb, rs = di.sample_rows(w, 16)
+    ref = oracle.attention_rows(qb, kb, vb, w.scale, rb, rs)
+    mass = oracle.attention_rows(qb, kb, abs_bits(vb), w.scale, rb, rs)
+    Sl = w.S // w.P
+    got = np.stack([torch_to_f64(outs[int(s) // Sl][int(b), int(s) % Sl]) for b, s in zip(rb, rs)])
+    assert_close(got, ref, mass, "max_s_d64")
