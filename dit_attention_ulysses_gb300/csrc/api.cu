@@ -508,7 +508,8 @@ int noalloc_scratch(void** out) {
 
 // Streams and events of the host-buffer pipeline (xs_attn_a2a_fwd_staged):
 // created once per device on first use and kept for the life of the process.
-constexpr int PIPE_MAX_GROUPS = 8;
+constexpr int PIPE_BASE_GROUPS = 8;                     // equal head groups of the host-buffer pipeline,
+constexpr int PIPE_MAX_GROUPS = PIPE_BASE_GROUPS + 2;   // the first and the last halved
 struct PipeStreams {
     bool ready = false;
     std::mutex mutex;
@@ -912,7 +913,20 @@ int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v
     // Head groups: the copies of group g + 1 in and of group g - 1 out overlap the
     // kernel of group g.  Every copy is one pitched cudaMemcpy2DAsync: the group's
     // heads are hg * D contiguous elements of every [.., H, D] row.
-    const int ng = H < PIPE_MAX_GROUPS ? H : PIPE_MAX_GROUPS;
+    // Group bounds: PIPE_BASE_GROUPS equal groups, the first and the last cut in
+    // two, since their copies (the first group's in, the last group's out) are the
+    // ones no kernel hides.
+    int bounds[PIPE_MAX_GROUPS + 1];
+    int ng = 0;
+    {
+        const int nb = H < PIPE_BASE_GROUPS ? H : PIPE_BASE_GROUPS;
+        bounds[0] = 0;
+        for (int i = 0; i < nb; ++i) {
+            const int lo = H * i / nb, hi = H * (i + 1) / nb;
+            if (nb >= 2 && (i == 0 || i == nb - 1) && hi - lo >= 2) bounds[++ng] = lo + (hi - lo) / 2;
+            bounds[++ng] = hi;
+        }
+    }
     const size_t row = static_cast<size_t>(H) * D * 2;       // bytes per (b, s) row
     const size_t rows_in = static_cast<size_t>(B) * S, rows_out = static_cast<size_t>(B) * (S / P);
     cudaError_t e;
@@ -922,7 +936,7 @@ int xs_attn_a2a_fwd_staged(const void* q_host, const void* k_host, const void* v
     const void* hin[3] = {q_host, k_host, v_host};
     void* din[3] = {q_dev, k_dev, v_dev};
     for (int g = 0; g < ng; ++g) {
-        const int h_lo = H * g / ng, h_hi = H * (g + 1) / ng;
+        const int h_lo = bounds[g], h_hi = bounds[g + 1];
         const size_t off = static_cast<size_t>(h_lo) * D * 2, width = static_cast<size_t>(h_hi - h_lo) * D * 2;
         for (int t = 0; t < 3; ++t)
             if ((e = cudaMemcpy2DAsync(static_cast<char*>(din[t]) + off, row, static_cast<const char*>(hin[t]) + off,

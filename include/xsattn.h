@@ -214,7 +214,9 @@ int xs_relayout_a2a_inverse(const void* const* seq_shards, void* const* heads,
  * Copies q, k, v from host memory into the caller's device buffers q_dev,
  * k_dev, v_dev, runs the fused kernel into the caller's device shards
  * out_dev[p], and copies every shard back into the host buffers out_host[p].
- * The work is pipelined over min(H, 8) groups of heads: the kernel of group g
+ * The work is pipelined over groups of heads (min(H, 8) equal groups, the first
+ * and the last cut in two, since their copies are the ones no kernel hides; up
+ * to 10 groups): the kernel of group g
  * runs on `stream` while the host-to-device copies of group g + 1 run on one
  * library stream and the device-to-host copies of group g - 1 on another (one
  * pitched cudaMemcpy2DAsync per tensor and group: a group's heads are a
