@@ -178,7 +178,9 @@ def test_deterministic(xs):
 
 
 def test_staged_host_entry_matches_device_entry(xs):
-    """The host-buffer entry pipelines min(H, 8) head groups (copies of the next
+    """The host-buffer entry pipelines head groups (min(H, 8) equal groups, the
+    first and the last halved where they hold two heads or more: here, 12 heads,
+    eight groups of one or two heads, the last one cut in two; copies of the next
     group in, kernel of this one, copies of the last one out, on three streams);
     without a workspace every group runs whole tiles, whose arithmetic is the
     whole-tensor kernel's, so the shards agree bit for bit.  Two calls back to
